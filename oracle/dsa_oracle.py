@@ -1,0 +1,257 @@
+"""Float64 CPU oracle for the DeepSeek Sparse Attention (DSA) forward path.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and bench.py's
+CPU-baseline leg may import or run this module; the product path never does.
+It shares no code with the CUDA library: it takes plain tensors/arrays drawn by
+dsa_workloads and writes everything it computes itself, in float64, one query at
+a time, in the order the method is described.  A library primitive (matrix
+product, sort, exp/log) serves as a step; nothing is blocked, fused or
+reordered beyond the definitions below.
+
+What is computed, and where it is defined:
+
+  lightning indexer   I[t, s] = sum_h w[t, h] * max(0, q_I[t, h, :] . k_I[s, :]),
+                      for the causal positions s <= p_t.
+                      "How GLM5.3 Sparse Attention Affects HBM Memory Usage",
+                      How it works / Model, first bullet (down-projected ReLU
+                      dot product, summed with weights across heads; selection
+                      shared by all attention heads); "DeepSeek Sparse
+                      Attention", In the code table ("ReLU(q.k) weighted sums").
+  top-k selection     the k causal positions with the largest I[t, .]; when the
+                      context holds at most k tokens every token is selected
+                      ("How GLM5.3 ...", Model, second bullet: top-k 2048,
+                      attention below 2K stays dense).  Equal scores are ordered
+                      by lower position first; -0.0 equals +0.0.
+  sparse MLA (MQA)    for each head h: z_s = scale * Q[t, h, :D] . C[s, :D] over
+                      the selected s; p = softmax(z); O[t, h, :] = sum_s p_s
+                      C[s, :D_v]; LSE = log sum_s exp(z_s).  All heads share the
+                      one latent row per token ("How GLM5.3 ...", Model, second
+                      bullet: sparse MLA in MQA mode).
+  IndexShare          one indexer + top-k per group of layers; every layer of
+                      the group attends over the same index set ("How GLM5.3
+                      ...", How it works / IndexShare: every 4 DSA layers share
+                      one indexer and the top-k indices are cached for reuse).
+
+Readings where the pages are silent (each one listed in the design doc):
+  * one indexer key per token, shared by all indexer heads;
+  * ReLU per head before weighting; weights unnormalised and may be negative;
+  * causality includes the query's own position (n_t = p_t + 1);
+  * value = the first D_v dims of the latent row; rope dims enter Q.K only;
+  * the returned index set is ascending, padded with -1 to k.
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+
+def bf16_to_f64(t: torch.Tensor) -> np.ndarray:
+    """Exact bf16 -> float64: a bf16 value is the top 16 bits of a float32."""
+    u16 = t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+    return (u16.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+
+def f32_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().numpy().astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# the three steps, for one query
+# ---------------------------------------------------------------------------
+
+def indexer_scores(q_idx: np.ndarray, w: np.ndarray, keys: np.ndarray) -> np.ndarray:
+    """Lightning-indexer score of every key for one query.
+
+    q_idx [H_I, d_I], w [H_I], keys [n, d_I] (float64) -> I [n].
+    Per head: ReLU of the dot product; then the weighted sum over heads.
+    ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", Model, lightning
+    indexer bullet.)
+    """
+    per_head = keys @ q_idx.T                 # [n, H_I]: q_I[h] . k_I[s]
+    per_head = np.maximum(per_head, 0.0)      # ReLU per head
+    return per_head @ w                       # sum_h w[h] * ReLU(.)
+
+
+def topk_select(scores: np.ndarray, k: int) -> np.ndarray:
+    """Positions of the k largest scores, ties to the lower position, ascending.
+
+    A context of at most k tokens is taken whole ("How GLM5.3 ...", Model:
+    attention below 2K tokens stays dense).  -0.0 and +0.0 compare equal.
+    """
+    n = scores.shape[0]
+    if n <= k:
+        return np.arange(n, dtype=np.int64)
+    pos = np.arange(n, dtype=np.int64)
+    order = np.lexsort((pos, -scores))       # primary: score descending; then position ascending
+    return np.sort(order[:k])
+
+
+def sparse_mla(q: np.ndarray, rows: np.ndarray, scale: float, d_v: int):
+    """Softmax attention of every head over the selected latent rows.
+
+    q [H, D], rows [m, D] (the selected latent rows) -> O [H, d_v], LSE [H].
+    MQA mode: all heads read the same rows; values are rows[:, :d_v].
+    An empty selection gives O = 0 and LSE = -inf.
+    """
+    H = q.shape[0]
+    if rows.shape[0] == 0:
+        return np.zeros((H, d_v)), np.full(H, -np.inf)
+    z = scale * (rows @ q.T)                  # [m, H]
+    m = z.max(axis=0)                         # [H]
+    e = np.exp(z - m)                         # [m, H]
+    Z = e.sum(axis=0)                         # [H]
+    O = (e.T @ rows[:, :d_v]) / Z[:, None]    # [H, d_v]
+    return O, m + np.log(Z)
+
+
+# ---------------------------------------------------------------------------
+# whole forward over a workload
+# ---------------------------------------------------------------------------
+
+def _rows_of(wl, b: int, positions: np.ndarray) -> np.ndarray:
+    """Pool rows holding tokens `positions` of sequence b (layout lookup)."""
+    if wl.page_table is not None:
+        ps = wl.spec.page_size
+        pt = wl.page_table[b].cpu().numpy().astype(np.int64)
+        return pt[positions // ps] * ps + positions % ps
+    return int(wl.seq_start[b]) + positions
+
+
+def _query_table(wl):
+    lens = wl.seq_lens.cpu().tolist()
+    cu = wl.cu_seqlens_q.cpu().tolist()
+    seq, pos = [], []
+    for b in range(len(lens)):
+        nq = cu[b + 1] - cu[b]
+        for i in range(nq):
+            seq.append(b)
+            pos.append(lens[b] - nq + i)
+    return seq, pos
+
+
+class Forward:
+    """Oracle results for selected queries of a workload.
+
+    idx[t]   ascending selected positions (int64, length min(n_t, k))
+    out[l][t], lse[l][t]  per layer attention output [H, D_v] and LSE [H]
+    scores[t]  float64 indexer scores over the causal context (None when dense)
+    indexer_calls  number of indexer evaluations (one per sparse query)
+    """
+
+    def __init__(self):
+        self.idx = {}
+        self.scores = {}
+        self.out = []
+        self.lse = []
+        self.indexer_calls = 0
+
+
+def dsa_forward(wl, queries: Optional[Sequence[int]] = None, layers: Optional[Sequence[int]] = None,
+                keep_scores: bool = False, kv_rows_fetch=None) -> Forward:
+    """Run indexer -> top-k -> sparse MLA for the chosen query tokens.
+
+    One indexer evaluation and one top-k per query serve every layer of the
+    IndexShare group ("How GLM5.3 ...", IndexShare).  `kv_rows_fetch(layer,
+    rows)` may supply latent rows (as a bf16 tensor) when a pool is too large
+    to copy whole to the host; by default rows are read from wl.kv[layer].
+    """
+    spec = wl.spec
+    seq, pos = _query_table(wl)
+    T = len(seq)
+    queries = range(T) if queries is None else list(queries)
+    layers = range(spec.n_layers) if layers is None else list(layers)
+    res = Forward()
+    res.out = [dict() for _ in range(spec.n_layers)]
+    res.lse = [dict() for _ in range(spec.n_layers)]
+    k_pool = wl.k_idx
+    for t in queries:
+        b, p = seq[t], pos[t]
+        n = p + 1                                         # causal: s <= p
+        if n <= spec.topk:
+            sel = np.arange(n, dtype=np.int64)
+        else:
+            rows = _rows_of(wl, b, np.arange(n, dtype=np.int64))
+            keys = bf16_to_f64(k_pool[torch.from_numpy(rows).to(k_pool.device)])
+            s = indexer_scores(bf16_to_f64(wl.q_idx[t]), f32_to_f64(wl.w[t]), keys)
+            res.indexer_calls += 1
+            if keep_scores:
+                res.scores[t] = s
+            sel = topk_select(s, spec.topk)
+        res.idx[t] = sel
+        rows = _rows_of(wl, b, sel)
+        for layer in layers:
+            if kv_rows_fetch is not None:
+                c = bf16_to_f64(kv_rows_fetch(layer, rows))
+            else:
+                pool = wl.kv[layer]
+                c = bf16_to_f64(pool[torch.from_numpy(rows).to(pool.device)])
+            o, l = sparse_mla(bf16_to_f64(wl.q[layer][t]), c, spec.scale, spec.d_v)
+            res.out[layer][t] = o
+            res.lse[layer][t] = l
+    return res
+
+
+def attention_on_set(wl, t: int, layer: int, sel: np.ndarray, kv_rows_fetch=None):
+    """Sparse MLA of query t over an externally supplied index set `sel`
+    (used to judge the GPU outputs on the GPU's own selection)."""
+    seq, pos = _query_table(wl)
+    b = seq[t]
+    sel = np.asarray(sel, dtype=np.int64)
+    sel = sel[sel >= 0]
+    rows = _rows_of(wl, b, sel)
+    if kv_rows_fetch is not None:
+        c = bf16_to_f64(kv_rows_fetch(layer, rows))
+    else:
+        pool = wl.kv[layer]
+        c = bf16_to_f64(pool[torch.from_numpy(rows).to(pool.device)])
+    return sparse_mla(bf16_to_f64(wl.q[layer][t]), c, wl.spec.scale, wl.spec.d_v)
+
+
+def scores_for_query(wl, t: int) -> np.ndarray:
+    """float64 indexer scores of query t over its whole causal context."""
+    seq, pos = _query_table(wl)
+    b, p = seq[t], pos[t]
+    rows = _rows_of(wl, b, np.arange(p + 1, dtype=np.int64))
+    keys = bf16_to_f64(wl.k_idx[torch.from_numpy(rows).to(wl.k_idx.device)])
+    return indexer_scores(bf16_to_f64(wl.q_idx[t]), f32_to_f64(wl.w[t]), keys)
+
+
+def band_check(oracle_scores: np.ndarray, k: int, gpu_sel: np.ndarray, rel_band: float = 1e-3):
+    """Compare a selection against the oracle scores with a tie band.
+
+    Every position whose oracle score lies above theta + band must be selected
+    and every one below theta - band must not be, where theta is the k-th
+    largest oracle score and band = rel_band * |theta|.  Returns a list of
+    violations (empty when the selection passes) and theta.
+    """
+    n = oracle_scores.shape[0]
+    sel = np.asarray(gpu_sel, dtype=np.int64)
+    sel = sel[sel >= 0]
+    problems = []
+    if n <= k:
+        if not np.array_equal(np.sort(sel), np.arange(n)):
+            problems.append("dense row is not 0..n-1")
+        return problems, math.nan
+    if sel.shape[0] != k:
+        problems.append(f"selected {sel.shape[0]} positions, expected {k}")
+    if np.unique(sel).shape[0] != sel.shape[0]:
+        problems.append("duplicate positions")
+    if sel.size and (sel.min() < 0 or sel.max() >= n):
+        problems.append("position outside the causal context")
+        return problems, math.nan
+    theta = np.sort(oracle_scores)[::-1][k - 1]
+    band = rel_band * abs(theta)
+    chosen = np.zeros(n, dtype=bool)
+    chosen[sel] = True
+    must = oracle_scores > theta + band
+    must_not = oracle_scores < theta - band
+    miss = np.nonzero(must & ~chosen)[0]
+    extra = np.nonzero(must_not & chosen)[0]
+    if miss.size:
+        problems.append(f"{miss.size} positions above the band not selected (e.g. {miss[:5].tolist()})")
+    if extra.size:
+        problems.append(f"{extra.size} positions below the band selected (e.g. {extra[:5].tolist()})")
+    return problems, theta

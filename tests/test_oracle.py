@@ -1,0 +1,300 @@
+"""Pins of the float64 oracle against facts that do not come from the oracle.
+
+Each test checks a closed form, an invariant, a special case that reduces to a
+library routine (torch's scaled_dot_product_attention in float64), a defining
+property checked by brute force, or a figure printed on the pages.  Each is
+chosen so that a plausible mistake (ReLU after the head sum, a transposed
+operand, a dropped scale, values taken from the wrong dims, ties broken the
+wrong way, an off-by-one in causality) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_workloads as W
+import oracle
+from long_context_lightning_gb300 import accounting
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- indexer ---
+
+def test_indexer_unit_query_reads_one_key_column():
+    # one head, weight 1, q = e_c  ->  I[s] = max(0, k[s, c])
+    keys = rng.standard_normal((50, 16))
+    for c in (0, 7, 15):
+        q = np.zeros((1, 16)); q[0, c] = 1.0
+        got = oracle.indexer_scores(q, np.array([1.0]), keys)
+        np.testing.assert_array_equal(got, np.maximum(keys[:, c], 0.0))
+
+
+def test_indexer_relu_is_per_head_before_weighting():
+    # heads q and -q with weights (1, 1): relu(x) + relu(-x) = |x|.
+    # A ReLU applied after the head sum would give relu(0) = 0 instead.
+    d = 8
+    a = rng.integers(-5, 6, size=d).astype(np.float64)
+    v = rng.integers(-5, 6, size=d).astype(np.float64)
+    keys = np.diag(a)                       # q . k_s = v[s] * a[s] without a matmul
+    q = np.stack([v, -v])
+    got = oracle.indexer_scores(q, np.array([1.0, 1.0]), keys)
+    np.testing.assert_array_equal(got, np.abs(v * a))
+    # a negative weight flips the sign of that head's (non-negative) term
+    got = oracle.indexer_scores(v[None, :], np.array([-2.0]), keys)
+    np.testing.assert_array_equal(got, -2.0 * np.maximum(v * a, 0.0))
+
+
+def test_indexer_linear_in_weights_homogeneous_in_query_equivariant_in_keys():
+    q = rng.standard_normal((6, 12)); keys = rng.standard_normal((40, 12))
+    w1 = rng.standard_normal(6); w2 = rng.standard_normal(6)
+    i1 = oracle.indexer_scores(q, w1, keys); i2 = oracle.indexer_scores(q, w2, keys)
+    np.testing.assert_allclose(oracle.indexer_scores(q, w1 + w2, keys), i1 + i2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.indexer_scores(2.0 * q, w1, keys), 2.0 * i1, rtol=1e-12, atol=1e-12)
+    perm = rng.permutation(40)
+    np.testing.assert_allclose(oracle.indexer_scores(q, w1, keys[perm]), i1[perm], rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_exact_on_integer_inputs_brute_force():
+    # tiny workload: integer q, k in [-3, 3], weights in {0.5, 1, 2}: exact
+    # rational arithmetic with python ints must agree bit for bit.
+    wl = W.make_workload(W.SPECS["tiny"])
+    t = 3
+    s = oracle.scores_for_query(wl, t)
+    q = wl.q_idx[t].float().tolist(); w = wl.w[t].tolist()
+    seq, pos = wl.query_positions()
+    for sp in (0, 1, 100, pos[t]):
+        k = wl.k_idx[int(wl.seq_start[0]) + sp].float().tolist()
+        exact = 0.0
+        for h in range(len(q)):
+            dot = sum(int(a) * int(b) for a, b in zip(q[h], k))
+            exact += w[h] * max(0, dot)
+        assert s[sp] == exact
+    assert np.all(s * 2 == np.round(s * 2))            # multiples of 0.5
+
+
+# ------------------------------------------------------------------ top-k ---
+
+def _check_topk_property(scores, k, sel):
+    n = scores.shape[0]
+    sel = np.asarray(sel)
+    assert np.all(np.diff(sel) > 0), "ascending, distinct"
+    if n <= k:
+        assert np.array_equal(sel, np.arange(n)); return
+    assert sel.shape[0] == k
+    chosen = np.zeros(n, bool); chosen[sel] = True
+    # brute force over all (selected, unselected) pairs
+    for s in np.nonzero(chosen)[0]:
+        for u in np.nonzero(~chosen)[0]:
+            assert scores[s] > scores[u] or (scores[s] == scores[u] and s < u)
+
+
+def test_topk_defining_property_with_many_ties():
+    for n, k in ((40, 7), (64, 64), (65, 64), (100, 1), (30, 50)):
+        scores = rng.integers(-3, 4, size=n).astype(np.float64)
+        _check_topk_property(scores, k, oracle.topk_select(scores, k))
+
+
+def test_topk_permutation_closed_form():
+    n, k = 1000, 37
+    scores = rng.permutation(n).astype(np.float64)
+    sel = oracle.topk_select(scores, k)
+    np.testing.assert_array_equal(sel, np.nonzero(scores >= n - k)[0])
+
+
+def test_topk_all_equal_takes_lowest_positions_and_signed_zero_ties():
+    np.testing.assert_array_equal(oracle.topk_select(np.full(100, 2.5), 10), np.arange(10))
+    z = np.zeros(20); z[::2] = -0.0                 # -0.0 == +0.0: ties by position
+    assert np.signbit(z[0])
+    np.testing.assert_array_equal(oracle.topk_select(z, 5), np.arange(5))
+
+
+def test_topk_dense_when_context_fits():
+    # "attention below 2K tokens stays dense": n <= k selects every position
+    np.testing.assert_array_equal(oracle.topk_select(rng.standard_normal(2048), 2048), np.arange(2048))
+    assert oracle.topk_select(rng.standard_normal(2049), 2048).shape == (2048,)
+
+
+# ------------------------------------------------------------- sparse MLA ---
+
+def _sdpa_f64(q, rows, scale, d_v, mask=None):
+    # torch's attention routine in float64: q [H, D], keys = rows, values = rows[:, :d_v]
+    Q = torch.from_numpy(q)[None, :, None, :]                      # [1, H, 1, D]
+    K = torch.from_numpy(rows)[None, None].expand(1, q.shape[0], -1, -1)
+    V = torch.from_numpy(rows[:, :d_v].copy())[None, None].expand(1, q.shape[0], -1, -1)
+    am = None if mask is None else torch.from_numpy(mask)[None, None, None, :]
+    out = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=am, scale=scale)
+    return out[0, :, 0, :].numpy()
+
+
+def test_mla_dense_case_equals_library_attention():
+    # k >= n: the selection is the whole causal context, so sparse MLA must be
+    # dense MQA softmax attention
+    H, D, Dv, n = 8, 80, 64, 37
+    q = rng.standard_normal((H, D)); rows = rng.standard_normal((n, D))
+    o, lse = oracle.sparse_mla(q, rows, 1 / math.sqrt(D), Dv)
+    np.testing.assert_allclose(o, _sdpa_f64(q, rows, 1 / math.sqrt(D), Dv), rtol=1e-12, atol=1e-12)
+    z = (rows @ q.T) / math.sqrt(D)
+    np.testing.assert_allclose(lse, np.log(np.exp(z).sum(0)), rtol=1e-12)
+
+
+def test_mla_equals_dense_attention_with_additive_mask():
+    # the model-code formulation ("DeepSeek Sparse Attention", In the code:
+    # the top-k set turned into an additive mask over dense attention)
+    H, D, Dv, n = 4, 64, 48, 90
+    q = rng.standard_normal((H, D)); rows = rng.standard_normal((n, D))
+    sel = np.sort(rng.choice(n, size=23, replace=False))
+    mask = np.full(n, -np.inf); mask[sel] = 0.0
+    o, _ = oracle.sparse_mla(q, rows[sel], 0.125, Dv)
+    np.testing.assert_allclose(o, _sdpa_f64(q, rows, 0.125, Dv, mask), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_closed_forms():
+    H, D, Dv = 3, 16, 8
+    rows = rng.standard_normal((10, D))
+    # Q = 0: uniform weights -> mean of the value dims (the FIRST Dv dims); LSE = log m
+    o, lse = oracle.sparse_mla(np.zeros((H, D)), rows, 0.5, Dv)
+    for h in range(H):
+        np.testing.assert_allclose(o[h], rows[:, :Dv].mean(0), rtol=1e-12)
+    np.testing.assert_allclose(lse, np.log(10.0))
+    # one selected row: output is its value, LSE is its logit
+    q = rng.standard_normal((H, D))
+    o, lse = oracle.sparse_mla(q, rows[4:5], 0.5, Dv)
+    np.testing.assert_allclose(o, np.repeat(rows[4:5, :Dv], H, 0), rtol=1e-12)
+    # two rows along unit directions: weights e^{s*x1} : e^{s*x2} (pins the scale)
+    r = np.zeros((2, D)); r[0, 0] = 1.0; r[1, 1] = 1.0; r[0, D - 1] = 5.0; r[1, D - 1] = -5.0
+    qq = np.zeros((1, D)); qq[0, 0] = 3.0; qq[0, 1] = 1.0
+    scale = 0.7
+    o, lse = oracle.sparse_mla(qq, r, scale, D)
+    a, b = math.exp(scale * 3.0), math.exp(scale * 1.0)
+    np.testing.assert_allclose(o[0], (a * r[0] + b * r[1]) / (a + b), rtol=1e-12)
+    np.testing.assert_allclose(lse[0], math.log(a + b), rtol=1e-12)
+
+
+def test_mla_invariants():
+    H, D, Dv = 5, 32, 24
+    q = rng.standard_normal((H, D)); rows = rng.standard_normal((17, D))
+    o, lse = oracle.sparse_mla(q, rows, 0.3, Dv)
+    perm = rng.permutation(17)
+    o2, lse2 = oracle.sparse_mla(q, rows[perm], 0.3, Dv)
+    np.testing.assert_allclose(o, o2, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, lse2, rtol=1e-12)
+    lo = rows[:, :Dv].min(0); hi = rows[:, :Dv].max(0)
+    assert np.all(o >= lo - 1e-12) and np.all(o <= hi + 1e-12)    # convex combination
+    same = np.repeat(rows[:1], 6, 0)
+    o3, _ = oracle.sparse_mla(q, same, 0.3, Dv)
+    np.testing.assert_allclose(o3, np.repeat(rows[:1, :Dv], H, 0), rtol=1e-12)
+    o4, lse4 = oracle.sparse_mla(q, rows[:0], 0.3, Dv)
+    assert np.all(o4 == 0) and np.all(np.isneginf(lse4))
+
+
+# ----------------------------------------------------------- whole forward ---
+
+def test_forward_tiny_dense_when_context_within_k():
+    spec = W.SPECS["tiny"].scaled(ctx_len=60, q_per_seq=4)       # n <= 64 = k for every query
+    wl = W.make_workload(spec)
+    res = oracle.dsa_forward(wl)
+    assert res.indexer_calls == 0
+    seq, pos = wl.query_positions()
+    for t in range(wl.total_q):
+        np.testing.assert_array_equal(res.idx[t], np.arange(pos[t] + 1))
+        # equals dense causal attention computed by the library routine
+        rows = oracle.bf16_to_f64(wl.kv[0][: pos[t] + 1])
+        ref = _sdpa_f64(oracle.bf16_to_f64(wl.q[0][t]), rows, spec.scale, spec.d_v)
+        np.testing.assert_allclose(res.out[0][t], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_forward_causality_excludes_future_and_includes_self():
+    wl = W.make_workload(W.SPECS["tiny"])
+    res = oracle.dsa_forward(wl, keep_scores=True)
+    seq, pos = wl.query_positions()
+    for t in range(wl.total_q):
+        assert res.scores[t].shape == (pos[t] + 1,)             # s = 0..p_t
+        _check_topk_property(res.scores[t], 64, res.idx[t])
+        assert res.idx[t].max() <= pos[t]
+
+
+def test_indexshare_scores_once_for_the_group():
+    # "How GLM5.3 ...", IndexShare: one indexer for 4 layers -> 75% fewer
+    # indexer evaluations; every layer attends over the same index set
+    spec = W.SPECS["indexshare"].scaled(ctx_len=3000, topk=256, heads=4, d_qk=80, d_v=64, idx_heads=4,
+                                        idx_dim=32, batch=2)
+    wl = W.make_workload(spec)
+    res = oracle.dsa_forward(wl)
+    assert res.indexer_calls == wl.total_q                        # not 4 x
+    for layer in range(4):
+        for t in range(wl.total_q):
+            o, l = oracle.attention_on_set(wl, t, layer, res.idx[t])
+            np.testing.assert_array_equal(o, res.out[layer][t])
+    # per layer, indexer work is 1/4 of one-indexer-per-layer: the page's -75%
+    assert 1 - res.indexer_calls / (4 * wl.total_q) == pytest.approx(0.75)
+
+
+def test_paged_layout_same_as_contiguous():
+    spec = W.SPECS["ragged"].scaled(batch=3, ctx_range=(100, 700), topk=128, heads=4, d_qk=80, d_v=64,
+                                    idx_heads=4, idx_dim=32)
+    wl = W.make_workload(spec)
+    # rebuild the same token content in a contiguous pool
+    seq, pos = wl.query_positions()
+    lens = wl.seq_lens.tolist()
+    start = np.concatenate([[0], np.cumsum(lens)[:-1]]).astype(np.int64)
+    rows = np.concatenate([W.pool_rows(wl, b, torch.arange(L)).numpy() for b, L in enumerate(lens)])
+    r = torch.from_numpy(rows)
+    contig = W.Workload(spec=spec.scaled(paged=False), seq_lens=wl.seq_lens, cu_seqlens_q=wl.cu_seqlens_q,
+                        q_idx=wl.q_idx, w=wl.w, k_idx=wl.k_idx[r], q=wl.q, kv=[wl.kv[0][r]],
+                        seq_start=torch.from_numpy(start))
+    a = oracle.dsa_forward(wl); b = oracle.dsa_forward(contig)
+    for t in range(wl.total_q):
+        np.testing.assert_array_equal(a.idx[t], b.idx[t])
+        np.testing.assert_array_equal(a.out[0][t], b.out[0][t])
+
+
+def test_band_check_accepts_exact_and_rejects_wrong():
+    s = rng.standard_normal(500)
+    sel = oracle.topk_select(s, 50)
+    assert oracle.band_check(s, 50, sel)[0] == []
+    bad = sel.copy(); bad[0] = int(np.argmin(s))
+    assert oracle.band_check(s, 50, np.sort(bad))[0] != []
+
+
+# ------------------------------------------------------ printed figures -----
+
+def test_page_figures_golden():
+    with open(os.path.join(GOLDEN, "page_figures.json")) as f:
+        g = json.load(f)
+    # 64 query heads, 576-d latent with 512-d values: decode intensity vs the
+    # page's 120.8 FLOP/B
+    got = accounting.decode_intensity(g["query_heads"]["value"], 576, 512)
+    assert got == pytest.approx(g["decode_intensity_flop_per_byte"]["value"], rel=1e-3)
+    assert W.SPECS["decode"].topk == g["index_topk"]["value"]
+    assert W.SPECS["indexshare"].n_layers == g["indexshare_group"]["value"]
+    assert W.SPECS["decode"].idx_heads == g["index_n_heads"]["value"]
+    assert W.SPECS["decode"].idx_dim == g["index_head_dim"]["value"]
+
+
+def test_tiny_golden_indices():
+    # regression pin: written by tests/golden/make_golden.py from the oracle
+    with open(os.path.join(GOLDEN, "tiny_topk.json")) as f:
+        g = json.load(f)
+    wl = W.make_workload(W.SPECS["tiny"])
+    res = oracle.dsa_forward(wl)
+    for t, row in enumerate(g["idx"]):
+        assert res.idx[t].tolist() == row
+
+
+def test_workload_recipe():
+    wl = W.make_workload(W.SPECS["tiny"])
+    seq, pos = wl.query_positions()
+    assert pos == list(range(496, 512))
+    again = W.make_workload(W.SPECS["tiny"])
+    assert torch.equal(wl.k_idx, again.k_idx) and torch.equal(wl.kv[0], again.kv[0])
+    assert set(torch.unique(wl.w).tolist()) <= {0.5, 1.0, 2.0}
+    assert int(wl.q_idx.float().abs().max()) <= 3
+    sp = W.SPECS["ragged"].scaled(batch=5, ctx_range=(100, 300))
+    wr = W.make_workload(sp)
+    allrows = torch.cat([W.pool_rows(wr, b, torch.arange(int(L))) for b, L in enumerate(wr.seq_lens.tolist())])
+    assert torch.unique(allrows).numel() == allrows.numel()       # pages never overlap
