@@ -1,0 +1,235 @@
+/*
+ * dsa.h -- C ABI of the DeepSeek Sparse Attention (DSA) forward path on one
+ * GB300 GPU (sm_103a).
+ *
+ * The path has three steps, each exported on its own and fused in dsa_forward:
+ *
+ *   1. lightning indexer: for query token t and past token s <= p_t,
+ *        I[t, s] = sum_h w[t, h] * max(0, q_I[t, h, :] . k_I[s, :])
+ *      ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
+ *      Model, lightning-indexer bullet: a down-projected ReLU dot product summed
+ *      with weights across heads; "DeepSeek Sparse Attention", In the code
+ *      table: "ReLU(q.k) weighted sums", index_n_heads / index_head_dim).
+ *   2. top-k: the k past tokens with the largest I[t, .]; when the causal
+ *      context holds at most k tokens, all of them ("How GLM5.3 ...", Model,
+ *      sparse-MLA bullet: top-k 2048, attention below 2K stays dense).  Equal
+ *      scores go to the lower position; -0.0 equals +0.0.
+ *   3. sparse MLA in MQA mode: every attention head attends with softmax over
+ *      the selected latent rows only; all heads read the same 576-dim latent
+ *      row of a token, the value is its first d_v dims ("How GLM5.3 ...",
+ *      Model, sparse-MLA bullet).
+ *   IndexShare: one indexer + top-k serves a group of layers, each attending
+ *   over the same index set with its own query and latent cache ("How GLM5.3
+ *   ...", How it works / IndexShare: every 4 DSA layers share one indexer and
+ *   the top-k indices are cached for the shared layers).
+ *
+ * Conventions shared by every call
+ *   - All pointers named "device" are CUDA device pointers of the current
+ *     device; the caller allocates, owns and frees every buffer.  The library
+ *     never allocates, frees or synchronises inside a compute call; every
+ *     compute call is asynchronous on `stream` and launches only kernels.
+ *   - Data types are fixed: bf16 (raw 16-bit storage, `const void*`) for
+ *     queries, caches and attention outputs; fp32 for head weights, scores and
+ *     LSE; int32 for lengths, page tables and selected positions.
+ *   - Every device pointer must be 16-byte aligned; every row stride is in
+ *     elements and must make rows 16-byte aligned.
+ *   - Ragged batches: sequence b has seq_lens_k[b] cached tokens, and its
+ *     queries are its LAST cu_seqlens_q[b+1]-cu_seqlens_q[b] positions, so
+ *     query i of b sits at position p = seq_lens_k[b] - nq_b + i and sees the
+ *     causal context s = 0..p (n_t = p + 1 tokens, its own position included).
+ *
+ * Errors
+ *   - Host-side checks (null pointers, alignment, unsupported sizes, a
+ *     workspace that is too small) return DSA_ERR_INVALID_ARG,
+ *     DSA_ERR_UNSUPPORTED or DSA_ERR_WORKSPACE and launch nothing.
+ *   - A failed launch returns DSA_ERR_CUDA.
+ *   - Device-side problems never trap: a bad length, page id or index is
+ *     skipped (the affected row is left unspecified) and a bounded wait that
+ *     runs out ends its block early; both set a device error word that
+ *     dsa_check_device_error() reports (DSA_ERR_BAD_INDEX / DSA_ERR_TIMEOUT)
+ *     and clears.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,  /* null pointer, misalignment, inconsistent sizes */
+  DSA_ERR_UNSUPPORTED = 2,  /* sizes outside the supported set (see below) */
+  DSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
+  DSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  DSA_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
+  DSA_ERR_BAD_INDEX = 6     /* a device-side length, page id or index was out of range */
+} dsa_status_t;
+
+typedef enum { DSA_CACHE_CONTIGUOUS = 0, DSA_CACHE_PAGED = 1 } dsa_cache_kind_t;
+
+/*
+ * A per-token row cache (indexer keys, or MLA latent rows) held in one pool of
+ * rows.  Row r starts at  (bf16*)base + r * row_stride.
+ *   contiguous: token s of sequence b is row seq_start[b] + s.
+ *   paged:      token s of sequence b is row
+ *                 page_table[b * page_table_stride + s / page_size] * page_size
+ *                 + s % page_size.
+ * Pages of a sequence beyond ceil(seq_lens_k[b] / page_size) are never read.
+ */
+typedef struct {
+  int32_t kind;               /* dsa_cache_kind_t */
+  int32_t page_size;          /* paged only: 64 */
+  const void* base;           /* device, bf16 row pool */
+  int64_t row_stride;         /* elements between rows (multiple of 8) */
+  int64_t num_rows;           /* rows in the pool; a row id >= num_rows is a bad index */
+  const int64_t* seq_start;   /* contiguous: device [num_seqs] */
+  const int32_t* page_table;  /* paged: device [num_seqs, page_table_stride] */
+  int64_t page_table_stride;  /* paged: entries per sequence */
+} dsa_cache_t;
+
+/* A ragged batch of query tokens. */
+typedef struct {
+  int32_t num_seqs;             /* B >= 1 */
+  int32_t total_q;              /* T = cu_seqlens_q[B] (host copy, sizes the grids) */
+  int32_t max_seqlen_k;         /* host upper bound of seq_lens_k[b] */
+  int32_t max_q_per_seq;        /* host upper bound of cu_seqlens_q[b+1]-cu_seqlens_q[b] */
+  const int32_t* cu_seqlens_q;  /* device [B+1], cu[0] = 0, non-decreasing */
+  const int32_t* seq_lens_k;    /* device [B], nq_b <= seq_lens_k[b] <= max_seqlen_k */
+} dsa_batch_t;
+
+/* Lightning-indexer inputs.  Supported: n_heads in 1..64, head_dim in {32, 64, 128}. */
+typedef struct {
+  const void* q;       /* device bf16 [T, n_heads, head_dim], contiguous */
+  const float* w;      /* device fp32 [T, n_heads], contiguous */
+  dsa_cache_t k;       /* indexer keys: one head_dim bf16 row per token, shared by all heads */
+  int32_t n_heads;
+  int32_t head_dim;
+} dsa_indexer_t;
+
+/* One sparse-MLA layer.  Supported: n_heads in 1..64 and
+ * (d_qk, d_v) in {(80, 64), (576, 512)}. */
+typedef struct {
+  const void* q;       /* device bf16 [T, n_heads, d_qk], contiguous */
+  dsa_cache_t kv;      /* latent rows: d_qk bf16 per token; value = first d_v dims */
+  int32_t n_heads;
+  int32_t d_qk;
+  int32_t d_v;
+  float scale;         /* softmax scale applied to q . k */
+} dsa_mla_layer_t;
+
+/* Largest supported top-k and IndexShare group. */
+#define DSA_MAX_TOPK 2048
+#define DSA_MAX_LAYERS 4
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dsa_status_string(dsa_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word set by
+ * earlier kernels of this library on the current device.  Returns DSA_OK,
+ * DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT, or DSA_ERR_CUDA if the sync failed.
+ */
+dsa_status_t dsa_check_device_error(cudaStream_t stream);
+
+/*
+ * Bytes of device workspace the calls below need for `batch` and `topk`
+ * (a per-query plan plus, for dsa_forward, the fp32 score matrix
+ * [total_q, round_up(max_seqlen_k, 4)]).  0 on invalid arguments.
+ */
+size_t dsa_workspace_size(const dsa_batch_t* batch, int32_t topk);
+
+/*
+ * Step 1 alone: lightning-indexer scores.
+ *   scores  device fp32 [total_q, ld_scores], ld_scores >= max_seqlen_k,
+ *           multiple of 4.  Row t receives I[t, s] for s < n_t; entries
+ *           s >= n_t are not written.
+ *   skip_dense_k  queries with n_t <= skip_dense_k are skipped (their rows
+ *           are not written; pass 0 to score every query, or the top-k to
+ *           skip the rows dsa_topk takes whole).
+ *   workspace  device, >= dsa_workspace_size(batch, 0) bytes.
+ */
+dsa_status_t dsa_indexer_scores(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
+                                int32_t skip_dense_k, float* scores, int64_t ld_scores,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Step 2 alone: exact top-k per query row of `scores` (layout as above; only
+ * entries s < n_t are read).  Writes idx[t * ld_idx + j], j < topk: the
+ * selected positions in ascending order, then -1 padding when n_t < topk.
+ * topk in 1..2048.
+ */
+dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_scores, int32_t topk,
+                      int32_t* idx, int64_t ld_idx, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/*
+ * Step 3 alone: sparse MLA over caller-supplied positions.
+ *   idx    device int32 [total_q, ld_idx]; entry j < min(topk, n_t) of row t is
+ *          a position of t's sequence, or -1 (skipped).  Entries at
+ *          j >= min(topk, n_t) are never read.  A position outside [0, n_t)
+ *          is skipped and flagged DSA_ERR_BAD_INDEX.  Repeated positions count
+ *          as often as they appear.
+ *   out    device bf16 [total_q, n_heads, d_v].
+ *   lse    device fp32 [total_q, n_heads] (natural log of the softmax
+ *          denominator, scale included), or NULL.  A row with no valid
+ *          position gets out = 0 and lse = -inf.
+ */
+dsa_status_t dsa_sparse_mla_fwd(const dsa_batch_t* batch, const dsa_mla_layer_t* layer, const int32_t* idx,
+                                int64_t ld_idx, int32_t topk, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The fused forward: indexer (scores for the sparse queries only) -> top-k
+ * (dense rows filled directly) -> sparse MLA for each of the n_layers layers
+ * of an IndexShare group, all reading the one index set.
+ *   idx    device int32 [total_q, ld_idx], written once (the cached top-k).
+ *   outs   host array of n_layers device bf16 [total_q, n_heads, d_v] pointers.
+ *   lses   host array of n_layers device fp32 [total_q, n_heads] pointers
+ *          (entries may be NULL), or NULL.
+ *   workspace  device, >= dsa_workspace_size(batch, topk) bytes.
+ */
+dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
+                         int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                         void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/*
+ * dsa_forward with timing marks: identical work, plus cudaEventRecord of the
+ * caller's events on `stream` -- marks[0] before the first launch, marks[1]
+ * after the per-call plan, marks[2] after the indexer, marks[3] after the
+ * top-k, marks[4] after the sparse-MLA launch.  `marks` holds 5 events
+ * created by the caller (cudaEventDefault); NULL behaves like dsa_forward.
+ */
+dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
+                                int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                                void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream, cudaEvent_t const* marks);
+
+/*
+ * Self-checks of the library's own device machinery (test use).
+ *
+ * dsa_selftest_mma: one 128 x 64 tile D = A * B^T computed by the tensor-core
+ * path the kernels use (bf16 operands staged in swizzled shared memory, fp32
+ * accumulation in tensor memory).  A is bf16 [128, 64] row-major, B is bf16
+ * [64, 64] row-major, D fp32 [128, 64].  `a_mn_major` / `b_mn_major` stage the
+ * operand transposed (as the attention value and probability operands are).
+ *
+ * dsa_selftest_timeout: launches one block that waits on a barrier nobody
+ * arrives at; the bounded wait gives up after about `limit_ms` milliseconds
+ * and sets the device error word, which dsa_check_device_error then reports
+ * as DSA_ERR_TIMEOUT.  Nothing faults; the context stays usable.
+ */
+dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
+                              cudaStream_t stream);
+dsa_status_t dsa_selftest_timeout(int32_t limit_ms, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,72 @@
+"""Builds libdsa.so (the C-ABI library) in-tree for sm_103a with nvcc.
+
+Each translation unit compiles in parallel to an object under _build/, then
+one link produces long_context_lightning_gb300/libdsa.so.  No cmake, no
+torch extension machinery: the library has no Python or torch types in it.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(PKG, "csrc")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libdsa.so")
+SOURCES = ["dsa_api.cu", "plan.cu", "indexer.cu", "topk.cu", "sparse_mla.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the DSA library needs the CUDA toolkit to build")
+
+
+def _flags(extra=()):
+    return ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+            "-I", os.path.join(PKG, "..", "include"), *ARCH, *extra]
+
+
+def build(verbose: bool = False, ptxas_info: bool = False, jobs: int = 0) -> str:
+    """Compile every .cu file and link libdsa.so; returns the library path."""
+    nvcc = _nvcc()
+    os.makedirs(BUILD, exist_ok=True)
+    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    headers.append(os.path.join(PKG, "..", "include", "dsa.h"))
+    newest_header = max(os.path.getmtime(h) for h in headers)
+
+    def compile_one(src):
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        path = os.path.join(CSRC, src)
+        if (not ptxas_info and os.path.exists(obj)
+                and os.path.getmtime(obj) > max(os.path.getmtime(path), newest_header)):
+            return obj, ""
+        cmd = [nvcc, *_flags(extra), "-c", path, "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj, r.stdout + r.stderr
+
+    jobs = jobs or min(len(SOURCES), os.cpu_count() or 4)
+    with cf.ThreadPoolExecutor(jobs) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    for obj, log in results:
+        if log and (verbose or ptxas_info):
+            print(log, file=sys.stderr)
+    objs = [o for o, _ in results]
+    if (not os.path.exists(LIB)) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+        cmd = [nvcc, "-shared", *ARCH, "-o", LIB, *objs, "-lcuda"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True, ptxas_info="-v" in sys.argv))

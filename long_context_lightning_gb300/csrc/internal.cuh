@@ -1,0 +1,156 @@
+// internal.cuh -- definitions shared by the kernels and the host launchers of
+// the DSA library (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dsa.h"
+#include "ptx.cuh"
+
+namespace dsa {
+
+// Device view of a dsa_cache_t.
+struct CacheView {
+  const __nv_bfloat16* base;
+  int64_t row_stride;
+  int64_t num_rows;
+  const int64_t* seq_start;
+  const int32_t* page_table;
+  int64_t pt_stride;
+  int32_t page_size;
+  int32_t paged;
+};
+
+// Pool row of token s of sequence b, or -1 when the page id / row is out of range.
+__device__ __forceinline__ int64_t cache_row(const CacheView& c, int b, int64_t s) {
+  int64_t row;
+  if (c.paged) {
+    const int64_t page = s / c.page_size;
+    const int64_t phys = __ldg(c.page_table + (int64_t)b * c.pt_stride + page);
+    row = phys * c.page_size + (s - page * c.page_size);
+    if (phys < 0) return -1;
+  } else {
+    row = __ldg(c.seq_start + b) + s;
+  }
+  return (row >= 0 && row < c.num_rows) ? row : -1;
+}
+
+// ------------------------------------------------------------------ plan ---
+// Per-call plan written to the head of the workspace by plan_kernel:
+//   q_seq[T]  sequence of query t
+//   q_n[T]    causal context n_t = p_t + 1 (0 when its sequence is malformed)
+//   groups    consecutive queries of one sequence scored together by the
+//             indexer (G per group): g_info[g] = {b, first query, #queries,
+//             n of the group's last query}, g_tile_start[g] = first 128-key
+//             work item of group g (prefix sum), g_tile_start[n_groups] = total
+//   header    {n_groups, total_items}
+struct PlanView {
+  int32_t* header;       // [4]
+  int32_t* q_seq;        // [T]
+  int32_t* q_n;          // [T]
+  int4* g_info;          // [T]
+  int32_t* g_tile_start; // [T + 1]
+};
+
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline size_t plan_bytes(int64_t T) {
+  return align_up(16, 256) + align_up(4 * T, 256) * 2 + align_up(16 * T, 256) + align_up(4 * (T + 1), 256);
+}
+
+inline PlanView plan_view(void* ws, int64_t T) {
+  char* p = static_cast<char*>(ws);
+  PlanView v;
+  v.header = reinterpret_cast<int32_t*>(p);
+  p += align_up(16, 256);
+  v.q_seq = reinterpret_cast<int32_t*>(p);
+  p += align_up(4 * T, 256);
+  v.q_n = reinterpret_cast<int32_t*>(p);
+  p += align_up(4 * T, 256);
+  v.g_info = reinterpret_cast<int4*>(p);
+  p += align_up(16 * T, 256);
+  v.g_tile_start = reinterpret_cast<int32_t*>(p);
+  return v;
+}
+
+struct PlanParams {
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens_k;
+  int32_t B;
+  int32_t T;
+  int32_t max_seqlen_k;
+  int32_t group;        // G queries per indexer group
+  int32_t skip_dense_k; // groups whose every query has n <= skip are given no work
+  PlanView plan;
+  int* err;
+};
+
+constexpr int kIdxTileKeys = 128;  // keys per indexer work item (tcgen05 M)
+
+// Host launchers (each .cu file defines its own).
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+
+struct IndexerLaunch {
+  CacheView k;
+  const void* q;
+  const float* w;
+  int32_t H;
+  int32_t d;
+  int32_t T;
+  int32_t group;      // G
+  float* scores;
+  int64_t ld;
+  PlanView plan;
+  int* err;
+  int num_sms;
+};
+cudaError_t launch_indexer(const IndexerLaunch& a, cudaStream_t stream);
+
+struct TopkLaunch {
+  const float* scores;
+  int64_t ld_scores;
+  int32_t* idx;
+  int64_t ld_idx;
+  int32_t k;
+  int32_t T;
+  int32_t max_n;
+  const int32_t* q_n;
+  int* err;
+  int num_sms;
+};
+cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);
+
+struct MlaLayerView {
+  const __nv_bfloat16* q;
+  CacheView kv;
+  __nv_bfloat16* out;
+  float* lse;
+  float scale;
+  int32_t H;
+};
+struct MlaLaunch {
+  MlaLayerView layer[DSA_MAX_LAYERS];
+  int32_t n_layers;
+  int32_t d_qk;
+  int32_t d_v;
+  const int32_t* idx;
+  int64_t ld_idx;
+  int32_t k;
+  int32_t T;
+  int32_t max_n;
+  const int32_t* q_seq;
+  const int32_t* q_n;
+  int* err;
+  int num_sms;
+};
+cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
+
+// Tensor-map encoder (driver entry point, resolved once).
+CUresult encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
+                     const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                     CUtensorMapSwizzle swizzle);
+
+}  // namespace dsa

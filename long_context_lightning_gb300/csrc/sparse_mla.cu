@@ -1,0 +1,548 @@
+// sparse_mla.cu -- sparse MLA in MQA mode over the selected latent rows.
+//
+// For query t and head h, over the selected positions s:
+//   z_s = scale * Q[t, h, :D] . C[s, :D],  p = softmax(z),
+//   O[t, h, :] = sum_s p_s C[s, :D_v],  LSE[t, h] = log sum_s exp(z_s)
+// ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
+// Model, sparse-MLA bullet: sparse MLA in MQA mode over the top-k tokens, all
+// heads sharing the one latent row of a token).
+//
+// Layout of the work on the tensor cores.  128 selected rows are gathered into
+// shared memory as D/64 column blocks of [128 rows x 64 dims] (128-byte
+// swizzle).  The same bytes serve two MMAs:
+//   S^T[key, h] = C[key, :] . Q[h, :]^T     M = 128 keys, N = 64 heads, K = D
+//                 (C block K-major, Q block K-major)
+//   O^T[v, h]  += C[key, v]^T . P^T[key, h] M = 128 value dims per block, N = 64
+//                 heads, K = 128 keys (C block read MN-major, P MN-major)
+// so the 64-head MQA tile is a real dense contraction with every TMEM lane in
+// use (O^T: 4 x 64 columns, S^T: 64 columns).  One thread owns one key of S^T:
+// the per-head softmax max over the 128 keys is a 62-shuffle transpose
+// reduction per warp plus a 4-warp exchange; the running max is only raised
+// when a head's max grows by more than 2^8 (the exact result is unchanged,
+// only the reference point moves), so O^T is rarely rescaled in TMEM.
+//
+// Split over a cluster: the selected rows of one query are divided among the
+// blocks of a thread-block cluster; each block keeps its partial (m, l, O) and
+// the cluster combines them through distributed shared memory, so partial
+// outputs never travel through global memory.
+//
+// Warp roles (288 threads, one block per SM):
+//   warps 0..3  row gather: index -> pool row (paged or contiguous), 16-byte
+//               cp.async copies into the swizzled blocks, one barrier per block
+//   warp 4      TMEM owner, query TMA, MMA issuer (one thread)
+//   warps 5..8  softmax (one per TMEM lane quadrant), then the combine
+#include "internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // raise the running max only past 2^8
+
+template <int NB, int MB, bool PSEP>
+struct MlaCfg {
+  static constexpr int THREADS = 288;
+  static constexpr int BLK = 128 * 128;               // one [128 rows x 64 dims] block
+  static constexpr int OFF_Q = 0;                     // NB x [64 heads x 64 dims]
+  static constexpr int OFF_KV = OFF_Q + NB * 64 * 128;
+  static constexpr int OFF_P = PSEP ? OFF_KV + NB * BLK : OFF_KV + (NB - 1) * BLK;
+  static constexpr int OFF_ROWS = (PSEP ? OFF_P + BLK : OFF_KV + NB * BLK);  // 2 x 128 row pointers
+  static constexpr int OFF_VALID = OFF_ROWS + 2 * 128 * 8;                   // 2 x 128 int
+  static constexpr int OFF_RED = OFF_VALID + 2 * 128 * 4;                    // 4 x 64 float
+  static constexpr int OFF_MRUN = OFF_RED + 4 * 64 * 4;                      // 64 float
+  static constexpr int OFF_ALPHA = OFF_MRUN + 64 * 4;                        // 64 float
+  static constexpr int OFF_ML = OFF_ALPHA + 64 * 4;                          // 2 x 64 float (m, l)
+  static constexpr int OFF_F = OFF_ML + 2 * 64 * 4;                          // 64 float
+  static constexpr int OFF_BAR = OFF_F + 64 * 4;
+  static constexpr int N_BARS = 2 * NB + 5;
+  static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int TMEM_COLS = (MB * 64 + 64) <= 128 ? 128 : (MB * 64 + 64) <= 256 ? 256 : 512;
+  static constexpr int S_COL = MB * 64;
+  static_assert(PSEP || NB > 2 * MB, "P reuses the last column block only when no value block lives there");
+};
+
+struct MlaParams {
+  MlaLayerView layer[DSA_MAX_LAYERS];
+  int32_t d_qk;
+  int32_t d_v;
+  const int32_t* idx;
+  int64_t ld_idx;
+  int32_t k;
+  int32_t T;
+  const int32_t* q_seq;
+  const int32_t* q_n;
+  int* err;
+};
+
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+template <int NB, int MB, bool PSEP>
+__global__ void __launch_bounds__(288, 1)
+    sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
+                      const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_q3,
+                      MlaParams p) {
+  using C = MlaCfg<NB, MB, PSEP>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const __nv_bfloat16** rows_s = reinterpret_cast<const __nv_bfloat16**>(smem + C::OFF_ROWS);
+  int* valid_s = reinterpret_cast<int*>(smem + C::OFF_VALID);
+  float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
+  float* mrun_s = reinterpret_cast<float*>(smem + C::OFF_MRUN);
+  float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
+  float* ml_s = reinterpret_cast<float*>(smem + C::OFF_ML);
+  float* f_s = reinterpret_cast<float*>(smem + C::OFF_F);
+  float* obuf = reinterpret_cast<float*>(smem + C::OFF_KV);  // [64][d_v] after the last tile
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  auto bar_full = [&](int kb) { return smem_u32(bars + kb); };
+  auto bar_empty = [&](int kb) { return smem_u32(bars + NB + kb); };
+  const uint32_t bar_s_full = smem_u32(bars + 2 * NB);
+  const uint32_t bar_p_full = smem_u32(bars + 2 * NB + 1);
+  const uint32_t bar_q_full = smem_u32(bars + 2 * NB + 2);
+  const uint32_t bar_o_done = smem_u32(bars + 2 * NB + 3);
+  const uint32_t bar_drain = smem_u32(bars + 2 * NB + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t csize = cluster_nctarank();
+  const int t = blockIdx.y % p.T;
+  const int li = blockIdx.y / p.T;
+  const MlaLayerView& L = p.layer[li];
+  const CUtensorMap* tm_q = li == 0 ? &tm_q0 : li == 1 ? &tm_q1 : li == 2 ? &tm_q2 : &tm_q3;
+
+  const int n_t = p.q_n[t];
+  const int b = p.q_seq[t];
+  const int nvalid = min(n_t, p.k);
+  const int tiles = (nvalid + 127) / 128;
+  const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
+  const int my_tiles = j1 - j0;
+
+  if (threadIdx.x == 0) {
+    for (int kb = 0; kb < NB; ++kb) {
+      mbar_init(bar_full(kb), 128);
+      mbar_init(bar_empty(kb), 1);
+    }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_p_full, 128);
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_o_done, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x >= 160 && threadIdx.x < 224) mrun_s[threadIdx.x - 160] = -INFINITY;
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    // ---------------------------------------------------------- row gather
+    const int pt = threadIdx.x;              // 0..127
+    const int chunk = pt & 7;                // 16-byte chunk within a 128-byte row
+    const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
+    bool bad = false;
+    for (int jj = 0; jj < my_tiles; ++jj) {
+      const int j = j0 + jj;
+      const int par = jj & 1;
+      {  // row of key pt of this tile
+        const int e = j * 128 + pt;
+        int pos = e < nvalid ? __ldg(idx_row + e) : -1;
+        const __nv_bfloat16* src = nullptr;
+        if (pos >= n_t || pos < -1) {
+          atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          pos = -1;
+        }
+        if (pos >= 0) {
+          const int64_t r = cache_row(L.kv, b, pos);
+          if (r < 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          else src = L.kv.base + r * L.kv.row_stride;
+        }
+        rows_s[par * 128 + pt] = src;
+        valid_s[par * 128 + pt] = src != nullptr;
+      }
+      named_bar_sync(2, 128);
+      const uint32_t phase = jj & 1;
+#pragma unroll 1
+      for (int kb = 0; kb < NB; ++kb) {
+        bad |= !mbar_wait(bar_empty(kb), phase ^ 1, abort_flag, p.err);
+        if (!bad) {
+          const uint32_t dst0 = sbase + C::OFF_KV + kb * C::BLK;
+          const int col = kb * 64 + chunk * 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = (pt >> 3) + 16 * i;
+            const __nv_bfloat16* src = rows_s[par * 128 + r];
+            const bool ok = src != nullptr && col < p.d_qk;
+            cp_async_16(dst0 + r * 128 + ((chunk ^ (r & 7)) << 4), ok ? (const void*)(src + col) : (const void*)L.kv.base,
+                        ok ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        // signal the block issued two steps ago once its copies have landed
+        if (kb >= 2) {
+          cp_async_wait_group<2>();
+          fence_proxy_async_smem();
+          mbar_arrive(bar_full(kb - 2));
+        }
+      }
+      cp_async_wait_group<0>();
+      fence_proxy_async_smem();
+      for (int kb = (NB >= 2 ? NB - 2 : 0); kb < NB; ++kb) mbar_arrive(bar_full(kb));
+    }
+    cp_async_wait_all();
+  } else if (warp == 4) {
+    // ---------------------------------------------- query TMA + MMA issuer
+    if (lane == 0) {
+      bool bad = false;
+      if (my_tiles > 0) {
+        mbar_arrive_expect_tx(bar_q_full, NB * 64 * 128);
+        for (int kb = 0; kb < NB; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 64 * 128, tm_q, bar_q_full, kb * 64, 0, t);
+        bad = !mbar_wait(bar_q_full, 0, abort_flag, p.err);
+      }
+      constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
+      constexpr uint32_t idesc_o = mma_idesc_bf16(128, 64, true, true);
+      for (int jj = 0; jj < my_tiles && !bad; ++jj) {
+        const uint32_t phase = jj & 1;
+        // S^T = C . Q^T over all D/64 column blocks
+        for (int kb = 0; kb < NB && !bad; ++kb) {
+          if (!mbar_wait(bar_full(kb), phase, abort_flag, p.err)) { bad = true; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sbase + C::OFF_KV + kb * C::BLK + kk * 32, 16, 1024);
+            const uint64_t bd = smem_desc_sw128(sbase + C::OFF_Q + kb * 64 * 128 + kk * 32, 16, 1024);
+            mma_bf16(tmem + C::S_COL, ad, bd, idesc_s, (kb | kk) != 0);
+          }
+        }
+        if (bad) break;
+        mma_commit(bar_s_full);
+        for (int kb = 2 * MB; kb < NB; ++kb)
+          if (PSEP || kb != NB - 1) mma_commit(bar_empty(kb));  // blocks read by S only
+        // O^T += C^T . P^T over the 128 keys
+        if (!mbar_wait(bar_p_full, phase, abort_flag, p.err)) { bad = true; break; }
+        tc_fence_after();
+        for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sbase + C::OFF_KV + 2 * mb * C::BLK + kk * 2048, C::BLK, 1024);
+            const uint64_t bd = smem_desc_sw128(sbase + C::OFF_P + kk * 2048, C::BLK, 1024);
+            mma_bf16(tmem + mb * 64, ad, bd, idesc_o, (jj | kk) != 0);
+          }
+          mma_commit(bar_empty(2 * mb));
+          if (2 * mb + 1 < NB) mma_commit(bar_empty(2 * mb + 1));
+        }
+        if (!PSEP) mma_commit(bar_empty(NB - 1));
+      }
+      mma_commit(bar_o_done);
+      mma_commit(bar_drain);
+      mbar_wait_drain(bar_drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;        // key (S^T) or value dim (O^T) lane
+    const int st = threadIdx.x - 160;        // 0..127
+    const float c = L.scale * kLog2e;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    float lsum[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) lsum[h] = 0.f;
+    bool bad = false;
+    for (int jj = 0; jj < my_tiles; ++jj) {
+      const int par = jj & 1;
+      bad |= !mbar_wait(bar_s_full, par, abort_flag, p.err);
+      tc_fence_after();
+      float x[64];
+#pragma unroll
+      for (int c16 = 0; c16 < 4; ++c16) {
+        uint32_t r[16];
+        tmem_ld16(lane_base + C::S_COL + c16 * 16, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) x[c16 * 16 + j] = __uint_as_float(r[j]);
+      }
+      const bool kv = valid_s[par * 128 + row] != 0;
+#pragma unroll
+      for (int h = 0; h < 64; ++h) x[h] = kv ? x[h] * c : -INFINITY;
+      // per-head max over this warp's 32 keys: transpose reduction, lane l ends
+      // with heads 2l and 2l+1
+      float y[32];
+      {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float keep = hi ? x[32 + i] : x[i];
+          const float send = hi ? x[i] : x[32 + i];
+          y[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+      }
+#pragma unroll
+      for (int w = 8, n = 16; w >= 1; w >>= 1, n >>= 1) {
+        const bool hi = lane & w;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float keep = hi ? y[n + i] : y[i];
+          const float send = hi ? y[i] : y[n + i];
+          y[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+        }
+      }
+      red_s[quad * 64 + 2 * lane] = y[0];
+      red_s[quad * 64 + 2 * lane + 1] = y[1];
+      named_bar_sync(3, 128);
+      bool rescale = false;
+      if (st < 64) {
+        const float mt = fmaxf(fmaxf(red_s[st], red_s[64 + st]), fmaxf(red_s[128 + st], red_s[192 + st]));
+        const float mr = mrun_s[st];
+        float alpha = 1.f;
+        if (mt > mr + kRescaleLog2 || (mr == -INFINITY && mt > -INFINITY)) {
+          alpha = (mr == -INFINITY) ? 0.f : exp2f(mr - mt);
+          mrun_s[st] = mt;
+          rescale = mr != -INFINITY;
+        }
+        alpha_s[st] = alpha;
+      }
+      rescale = bar_red_or(4, 128, rescale);
+      // probabilities, running sums, P^T row (this key's 64 heads, bf16)
+      const uint32_t prow = sbase + C::OFF_P + row * 128;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        float pv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int h = cc * 8 + j;
+          pv[j] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - mrun_s[h]);  // no valid key yet: m is -inf too
+          lsum[h] = fmaf(lsum[h], alpha_s[h], pv[j]);
+        }
+        st_shared_v4(prow + ((cc ^ (row & 7)) << 4), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
+                     pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
+      }
+      fence_proxy_async_smem();
+      if (rescale && !bad) {
+        // move O^T to the new reference point: column h times alpha[h]
+        for (int mb = 0; mb < MB; ++mb) {
+#pragma unroll
+          for (int c16 = 0; c16 < 4; ++c16) {
+            uint32_t r[16];
+            tmem_ld16(lane_base + mb * 64 + c16 * 16, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha_s[c16 * 16 + j]);
+            tmem_st16(lane_base + mb * 64 + c16 * 16, r);
+          }
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_p_full);
+      named_bar_sync(3, 128);  // alpha_s / mrun_s are rewritten by the next tile
+    }
+    // l per head over this block's keys: transpose reduction of the lane sums
+    {
+      float y[32];
+      {
+        const bool hi = lane & 16;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float keep = hi ? lsum[32 + i] : lsum[i];
+          const float send = hi ? lsum[i] : lsum[32 + i];
+          y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+        }
+      }
+#pragma unroll
+      for (int w = 8, n = 16; w >= 1; w >>= 1, n >>= 1) {
+        const bool hi = lane & w;
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          const float keep = hi ? y[n + i] : y[i];
+          const float send = hi ? y[i] : y[n + i];
+          y[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+      }
+      red_s[quad * 64 + 2 * lane] = y[0];
+      red_s[quad * 64 + 2 * lane + 1] = y[1];
+      named_bar_sync(3, 128);
+      if (st < 64) {
+        ml_s[st] = mrun_s[st];
+        ml_s[64 + st] = red_s[st] + red_s[64 + st] + red_s[128 + st] + red_s[192 + st];
+      }
+    }
+    if (my_tiles > 0) bad |= !mbar_wait(bar_o_done, 0, abort_flag, p.err);
+    tc_fence_after();
+  }
+
+  // ------------------------------------------------- combine over the cluster
+  __syncthreads();
+  cluster_sync();  // (m, l) of every block visible
+  if (threadIdx.x >= 160 && threadIdx.x < 224) {
+    const int h = threadIdx.x - 160;
+    float M = -INFINITY;
+    for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + h), r)));
+    float Lsum = 0.f;
+    if (M != -INFINITY)
+      for (uint32_t r = 0; r < csize; ++r) {
+        const float m_r = ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + h), r));
+        const float l_r = ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + 64 + h), r));
+        if (m_r != -INFINITY) Lsum += l_r * exp2f(m_r - M);
+      }
+    const float m_own = ml_s[h];
+    f_s[h] = (Lsum > 0.f && m_own != -INFINITY) ? exp2f(m_own - M) / Lsum : 0.f;
+    if (crank == 0 && L.lse != nullptr && h < L.H)
+      L.lse[(int64_t)t * L.H + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
+  }
+  __syncthreads();
+  if (warp >= 5) {
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    for (int mb = 0; mb < MB; ++mb) {
+      const int v = mb * 128 + row;
+#pragma unroll
+      for (int c16 = 0; c16 < 4; ++c16) {
+        uint32_t r[16];
+        if (my_tiles > 0) {
+          tmem_ld16(lane_base + mb * 64 + c16 * 16, r);
+          tmem_wait_ld();
+        }
+        if (v < p.d_v) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int h = c16 * 16 + j;
+            obuf[h * p.d_v + v] = my_tiles > 0 ? __uint_as_float(r[j]) * f_s[h] : 0.f;
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  cluster_sync();  // every block's scaled partial output is in its shared memory
+  {
+    const int slice = p.d_v / (int)csize;    // value dims this block writes
+    const int v0 = (int)crank * slice;
+    const int per_h = slice / 4;
+    const int items = L.H * per_h;
+    for (int it = threadIdx.x; it < items; it += C::THREADS) {
+      const int h = it / per_h;
+      const int v = v0 + (it % per_h) * 4;
+      const uint32_t local = smem_u32(obuf + h * p.d_v + v);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t r = 0; r < csize; ++r) {
+        const float4 o = ld_dsmem_f32x4(dsmem_addr(local, r));
+        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+      }
+      uint2 packed;
+      packed.x = pack_bf16x2(acc.x, acc.y);
+      packed.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(L.out + ((int64_t)t * L.H + h) * p.d_v + v) = packed;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // peers are done reading this block's shared memory
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+int g_max_cluster_mla[2] = {0, 0};
+
+template <int NB, int MB, bool PSEP>
+cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
+  using C = MlaCfg<NB, MB, PSEP>;
+  auto kern = sparse_mla_kernel<NB, MB, PSEP>;
+  CUtensorMap tm[DSA_MAX_LAYERS];
+  for (int l = 0; l < DSA_MAX_LAYERS; ++l) {
+    const int ls = l < a.n_layers ? l : 0;
+    const uint64_t dims[3] = {(uint64_t)a.d_qk, (uint64_t)a.layer[ls].H, (uint64_t)a.T};
+    const uint64_t strides[2] = {(uint64_t)a.d_qk * 2, (uint64_t)a.d_qk * a.layer[ls].H * 2};
+    const uint32_t box[3] = {64u, 64u, 1u};
+    if (encode_tmap(&tm[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.layer[ls].q, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  if (g_max_cluster_mla[which] == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    g_max_cluster_mla[which] = 8;
+    cudaLaunchConfig_t probe = {};
+    probe.gridDim = dim3(16, 1, 1);
+    probe.blockDim = dim3(C::THREADS, 1, 1);
+    probe.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 16;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    probe.attrs = &at;
+    probe.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &probe) == cudaSuccess && nclusters > 0)
+      g_max_cluster_mla[which] = 16;
+    cudaGetLastError();
+  }
+  const int units = a.T * a.n_layers;
+  const int tiles_max = (std::min(a.k, a.max_n) + 127) / 128;
+  int c = 1;
+  while (c * 2 <= g_max_cluster_mla[which] && c * 2 <= tiles_max && (int64_t)units * c * 2 <= a.num_sms) c *= 2;
+  while (c > 1 && a.d_v % (4 * c) != 0) c /= 2;
+
+  MlaParams p;
+  for (int l = 0; l < DSA_MAX_LAYERS; ++l) p.layer[l] = a.layer[l < a.n_layers ? l : 0];
+  p.d_qk = a.d_qk;
+  p.d_v = a.d_v;
+  p.idx = a.idx;
+  p.ld_idx = a.ld_idx;
+  p.k = a.k;
+  p.T = a.T;
+  p.q_seq = a.q_seq;
+  p.q_n = a.q_n;
+  p.err = a.err;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c, units, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = c;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tm[0], tm[1], tm[2], tm[3], p);
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  if (a.d_qk == 576 && a.d_v == 512) return launch_t<9, 4, false>(a, stream, 0);
+  if (a.d_qk == 80 && a.d_v == 64) return launch_t<2, 1, true>(a, stream, 1);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

@@ -1,0 +1,100 @@
+"""Parity at the five workloads' full sizes, in the launch configuration the
+benchmark times (the same fused call, also replayed from a CUDA graph).
+
+Decode, ragged and IndexShare are judged on every query; the prefill chunk on
+a sample of queries (the oracle scores 131072 keys per query in float64).
+Properties that hold at any size (ascending distinct positions inside the
+causal context, finite outputs) are checked on every row.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dsa_workloads as W
+from helpers import judge_forward, make_sa
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from long_context_lightning_gb300 import _lib
+    return _lib
+
+
+def _rows_valid(wl, idx):
+    seq, pos = wl.query_positions()
+    idx = idx.cpu().numpy()
+    k = wl.spec.topk
+    for t in range(idx.shape[0]):
+        sel = idx[t][idx[t] >= 0]
+        n = pos[t] + 1
+        assert len(sel) == min(n, k), f"query {t}: {len(sel)} selected"
+        assert np.all(np.diff(sel) > 0) and sel[0] >= 0 and sel[-1] < n, f"query {t}"
+        assert np.all(idx[t][len(sel):] == -1)
+
+
+def test_tiny_full(lib):
+    wl = W.make_workload(W.SPECS["tiny"]).to("cuda")
+    idx, outs, lses = make_sa(wl).forward()
+    assert lib.check_device_error() == lib.DSA_OK
+    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q), exact_idx=True)
+
+
+def test_decode_full_graph_replay(lib):
+    spec = W.SPECS["decode"]
+    wl = W.make_workload(spec, device="cuda")
+    sa = make_sa(wl)
+    idx, outs, lses = sa.forward()
+    torch.cuda.synchronize()
+    first = (idx.clone(), outs[0].clone(), lses[0].clone())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        sa.forward()
+    sa.idx.fill_(-5)
+    sa.outs[0].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert lib.check_device_error() == lib.DSA_OK
+    # deterministic: the replay reproduces the direct call bit for bit
+    assert torch.equal(sa.idx, first[0]) and torch.equal(sa.outs[0], first[1]) and torch.equal(sa.lses[0], first[2])
+    _rows_valid(wl, sa.idx)
+    assert torch.isfinite(sa.outs[0].float()).all()
+    judge_forward(wl.to("cpu"), sa.idx, sa.outs, sa.lses, range(wl.total_q))
+
+
+def test_prefill_full_sampled(lib):
+    spec = W.SPECS["prefill"]
+    wl = W.make_workload(spec, device="cuda")
+    idx, outs, lses = make_sa(wl).forward()
+    torch.cuda.synchronize()
+    assert lib.check_device_error() == lib.DSA_OK
+    _rows_valid(wl, idx)
+    assert torch.isfinite(outs[0].float()).all()
+    rng = np.random.default_rng(2)
+    sample = sorted({0, 1, 2, 3, 4095, 4094, 2048, *rng.choice(4096, 9, replace=False).tolist()})
+    judge_forward(wl.to("cpu"), idx, outs, lses, sample)
+
+
+def test_ragged_paged_full(lib):
+    spec = W.SPECS["ragged"]
+    wl = W.make_workload(spec, device="cuda")
+    idx, outs, lses = make_sa(wl).forward()
+    torch.cuda.synchronize()
+    assert lib.check_device_error() == lib.DSA_OK
+    assert (wl.seq_lens <= spec.topk).any() and (wl.seq_lens > spec.topk).any()   # both paths exercised
+    _rows_valid(wl, idx)
+    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+
+
+def test_indexshare_full(lib):
+    spec = W.SPECS["indexshare"]
+    wl = W.make_workload(spec, device="cuda")
+    idx, outs, lses = make_sa(wl).forward()
+    torch.cuda.synchronize()
+    assert lib.check_device_error() == lib.DSA_OK
+    _rows_valid(wl, idx)
+    # keep the four 2.4 GB latent pools on the device; the oracle fetches the rows it needs
+    judge_forward(wl.to("cpu", kv_too=False), idx, outs, lses, range(wl.total_q))
