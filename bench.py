@@ -155,6 +155,20 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized() and \
+            torch.distributed.get_world_size() > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return units_per_rank * world * steps / (max_total_ms / 1e3)
+
+
 def _traffic_from_profile(kernel_file: str, summary: str):
     """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
     path = os.path.join(ROOT, "profiles", summary)
@@ -240,6 +254,10 @@ def run_gpu(args, rank, world, local_rank):
     # per-kernel times on the same stream (marks between the launches), same flushing
     n_brk = min(args.steps, 200)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_brk)]
+    for row in marks:          # torch creates the CUDA event on first record
+        for m in row:
+            m.record(stream)
+    torch.cuda.synchronize(dev)
     for i in range(n_brk):
         flush.fill_(i)
         _lib.forward_marked(sa.batch, sa.indexer, sa.topk, sa.layers, sa.idx, sa.outs, sa.lses, sa.workspace,
@@ -286,13 +304,10 @@ def run_gpu(args, rank, world, local_rank):
 
     # aggregate over ranks: max time
     T = wl.total_q
-    t_local = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_local, op=torch.distributed.ReduceOp.MAX)
-    total_ms, e2e_ms = float(t_local[0]), float(t_local[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
     if rank != 0:
         return
-    value = T * world * args.steps / (total_ms / 1e3)
+    value = job_throughput(T, world, args.steps, total_ms)
     hbm, tf, peak_kind = _peaks()
     shp = _shape(wl)
     idx_bytes = accounting.indexer_bytes(shp)

@@ -194,7 +194,10 @@ def forward_marked(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaL
     arr = (MlaLayer * n)(*layers)
     out_ptrs = (c_void_p * n)(*[_ptr(o) for o in outs])
     lse_ptrs = None if lses is None else (c_void_p * n)(*[_ptr(x) for x in lses])
-    ev = (c_void_p * 5)(*[m.cuda_event for m in marks])
+    handles = [m.cuda_event for m in marks]
+    if not all(handles):
+        raise ValueError("record each torch.cuda.Event once before passing it (torch creates it lazily)")
+    ev = (c_void_p * 5)(*handles)
     _check(load().dsa_forward_marked(ctypes.byref(batch), ctypes.byref(indexer), k, n, arr, _ptr(idx),
                                      idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream), ev),

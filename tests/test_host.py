@@ -1,0 +1,103 @@
+"""Host-side checks that need no GPU: the C ABI library builds, loads and
+exports every function include/dsa.h declares; the binding's structs match the
+header's; the byte/FLOP accounting and the benchmark's argument handling."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    from long_context_lightning_gb300 import _lib
+    return _lib
+
+
+def _declared_functions():
+    hdrs = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h")]
+    names = set()
+    for h in hdrs:
+        txt = open(h).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        for m in re.finditer(r"\b(?:dsa_status_t|size_t|const char\*)\s+(dsa_\w+)\s*\(", txt):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol(built):
+    lib = ctypes.CDLL(built.LIB_PATH)
+    declared = _declared_functions()
+    assert len(declared) >= 9
+    missing = [n for n in declared if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+    assert set(declared) == set(built.EXPORTS), "binding export list out of date with the header"
+
+
+def test_status_strings_without_gpu(built):
+    lib = built.load()
+    for s in range(7):
+        assert lib.dsa_status_string(s).decode().startswith("DSA_")
+
+
+def test_struct_layout_matches_header(built):
+    # sizes/offsets of the ctypes mirrors follow the C layout of dsa.h (LP64)
+    assert ctypes.sizeof(built.Cache) == 56
+    assert built.Cache.base.offset == 8 and built.Cache.page_table_stride.offset == 48
+    assert ctypes.sizeof(built.Batch) == 32
+    assert built.Indexer.k.offset == 16 and ctypes.sizeof(built.Indexer) == 80
+    assert built.MlaLayer.kv.offset == 8 and built.MlaLayer.scale.offset == 76
+
+
+def test_host_validation_without_gpu(built):
+    # a NULL batch is rejected before any CUDA call
+    lib = built.load()
+    assert lib.dsa_workspace_size(None, 2048) == 0
+    b = built.Batch(0, 0, 0, 0, None, None)       # num_seqs = 0 is invalid
+    assert lib.dsa_workspace_size(ctypes.byref(b), 2048) == 0
+    b = built.Batch(2, 2, 1000, 1, 16, 32)         # fake aligned pointers; sizing is host arithmetic
+    ws = lib.dsa_workspace_size(ctypes.byref(b), 2048)
+    assert ws >= 2 * 1000 * 4
+    st = lib.dsa_topk(ctypes.byref(b), None, 1000, 2048, None, 2048, None, 0, None)
+    assert st == built.DSA_ERR_INVALID_ARG
+    st = lib.dsa_topk(ctypes.byref(b), 16, 1000, 4096, 16, 4096, 16, 1 << 20, None)
+    assert st == built.DSA_ERR_UNSUPPORTED
+
+
+def test_accounting_matches_hand_counts():
+    from long_context_lightning_gb300 import accounting as A
+    s = A.Shape(n=[32768] * 32, seq_of=list(range(32)), idx_heads=64, idx_dim=128, topk=2048, heads=64,
+                d_qk=576, d_v=512)
+    # indexer: 32 x (32768 keys x 256 B + 64 x 128 x 2 + 64 x 4)
+    assert A.indexer_bytes(s) == 32 * (32768 * 256 + 16384 + 256)
+    assert A.indexer_flops(s) == 32 * 2 * 64 * 128 * 32768
+    # sparse MLA: 32 x (2048 x 1152 + Q 73728 + O 65536 + LSE 256 + idx 8192)
+    assert A.mla_bytes(s) == 32 * (2048 * 1152 + 73728 + 65536 + 256 + 8192)
+    assert A.mla_flops(s) == 32 * 2 * 64 * 2048 * 1088
+    # dense rows (n <= k) never touch the indexer
+    d = A.Shape(n=[100, 3000], seq_of=[0, 1], idx_heads=64, idx_dim=128, topk=2048, heads=64, d_qk=576, d_v=512)
+    assert A.indexer_flops(d) == 2 * 64 * 128 * 3000
+    # a chunk of queries of one sequence reads the keys once
+    p = A.Shape(n=[5000, 5001], seq_of=[0, 0], idx_heads=64, idx_dim=128, topk=2048, heads=64, d_qk=576, d_v=512)
+    assert A.indexer_bytes(p) == 5001 * 256 + 2 * (16384 + 256)
+
+
+def test_bench_reference_line_keys():
+    # the reference arm's JSON contract, checked on a tiny budget without a GPU
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="2")
+    code = ("import bench, dsa_workloads as W; bench.WORKLOAD='tiny'; "
+            "import argparse; a=argparse.Namespace(steps=1, warmup=1); bench.run_reference(a, 0, 1)")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "cpu_baseline", "e2e", "config", "dtype"):
+        assert k in line
+    assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
