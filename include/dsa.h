@@ -211,6 +211,30 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
                                 cudaStream_t stream, cudaEvent_t const* marks);
 
 /*
+ * dsa_sparse_mla_fwd_noalloc -- step 3 for callers that cannot provide any
+ * device memory beyond their inputs and outputs (a plugin interface that
+ * hands over only tensor pointers, or an engine whose device memory is all
+ * claimed by its own pool, where a cudaMalloc at call time fails or stalls).
+ * The pages describe no counterpart: this entry point exists for such callers.
+ *
+ * Same arguments, results and errors as dsa_sparse_mla_fwd, minus the
+ * workspace: the per-call plan lives in a static device array of the library
+ * (about 115 KB, held by every GPU that loads the library until exit).
+ *   - total_q may be at most DSA_NOALLOC_MAX_QUERIES; larger batches return
+ *     DSA_ERR_UNSUPPORTED without launching anything.
+ *   - The first call on a device looks up that array's device address (one
+ *     cudaGetSymbolAddress with the device current); make that first call
+ *     before capturing a stream into a CUDA graph.
+ *   - Nothing is allocated or freed, by the library or any library routine.
+ *   - All calls share the one array, which keeps the last call's plan (each
+ *     call rewrites every entry it reads).  Calls whose work overlaps on the
+ *     GPU (different streams, or host threads) race on it: serialise them.
+ */
+#define DSA_NOALLOC_MAX_QUERIES 4096
+dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_layer_t* layer, const int32_t* idx,
+                                        int64_t ld_idx, int32_t topk, void* out, float* lse, cudaStream_t stream);
+
+/*
  * Self-checks of the library's own device machinery (test use).
  *
  * dsa_selftest_mma: one 128 x 64 tile D = A * B^T computed by the tensor-core

@@ -25,7 +25,8 @@ MAX_LAYERS = 4
 
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
-           "dsa_selftest_timeout"]
+           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc"]
+NOALLOC_MAX_QUERIES = 4096
 
 
 class Cache(ctypes.Structure):
@@ -87,6 +88,9 @@ def load() -> ctypes.CDLL:
     lib.dsa_forward_marked.argtypes = [POINTER(Batch), POINTER(Indexer), c_int32, c_int32, POINTER(MlaLayer),
                                        c_void_p, c_int64, POINTER(c_void_p), POINTER(c_void_p), c_void_p, c_size_t,
                                        c_void_p, POINTER(c_void_p)]
+    lib.dsa_sparse_mla_fwd_noalloc.restype = c_int32
+    lib.dsa_sparse_mla_fwd_noalloc.argtypes = [POINTER(Batch), POINTER(MlaLayer), c_void_p, c_int64, c_int32,
+                                               c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_mma.restype = c_int32
     lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p]
     lib.dsa_selftest_timeout.restype = c_int32
@@ -173,6 +177,16 @@ def sparse_mla_fwd(batch: Batch, layer: MlaLayer, idx: torch.Tensor, k: int, out
                                      _ptr(out), _ptr(lse), _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream)),
            "dsa_sparse_mla_fwd")
+
+
+def sparse_mla_fwd_noalloc(batch: Batch, layer: MlaLayer, idx: torch.Tensor, k: int, out: torch.Tensor,
+                           lse: Optional[torch.Tensor], stream=None):
+    """sparse_mla_fwd for callers that can pass no workspace (the plan lives in
+    a static device array of the library; at most NOALLOC_MAX_QUERIES queries)."""
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    _check(load().dsa_sparse_mla_fwd_noalloc(ctypes.byref(batch), ctypes.byref(layer), _ptr(idx), idx.stride(0), k,
+                                             _ptr(out), _ptr(lse), _stream(stream)),
+           "dsa_sparse_mla_fwd_noalloc")
 
 
 def forward(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], idx: torch.Tensor,

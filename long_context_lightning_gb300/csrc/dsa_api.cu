@@ -443,6 +443,61 @@ dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
                             workspace_bytes, stream, nullptr);
 }
 
+}  // extern "C"
+
+// ------------------------------------------- sparse MLA without a workspace ---
+// Some callers cannot hand the library any device memory beyond their inputs
+// and outputs: a plugin interface that passes only tensor pointers, or an
+// engine whose device memory is entirely claimed by its own pool, so a
+// cudaMalloc at call time would fail (or stall the device).  For them the
+// per-call plan of dsa_sparse_mla_fwd lives in this file-scope array instead
+// of a workspace.  Every GPU that loads the library holds it until exit.
+namespace dsa {
+namespace {
+
+constexpr int kNoAllocMaxQ = DSA_NOALLOC_MAX_QUERIES;
+constexpr size_t kNoAllocScratchBytes = align_up(16, 256) + 2 * align_up(4 * (size_t)kNoAllocMaxQ, 256) +
+                                        align_up(16 * (size_t)kNoAllocMaxQ, 256) +
+                                        align_up(4 * (size_t)(kNoAllocMaxQ + 1), 256);
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* g_noalloc_ptr[kMaxDevices] = {};  // device address of g_noalloc_scratch, per device
+std::mutex g_noalloc_mu;
+
+// Once per device, with that device current: the host-side name of the array
+// is only a stand-in, so the kernels get the address the runtime reports.
+dsa_status_t noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return DSA_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_layer_t* layer, const int32_t* idx,
+                                        int64_t ld_idx, int32_t topk, void* out, float* lse, cudaStream_t stream) {
+  dsa_status_t s = check_batch(batch);
+  if (s != DSA_OK) return s;
+  if (batch->total_q > DSA_NOALLOC_MAX_QUERIES) return DSA_ERR_UNSUPPORTED;  // beyond the static scratch
+  if (plan_bytes(batch->total_q) > kNoAllocScratchBytes) return DSA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != DSA_OK) return s;
+  // The plan kernel rewrites every entry the attention kernel reads, so the
+  // previous call's contents need no clearing.
+  return dsa_sparse_mla_fwd(batch, layer, idx, ld_idx, topk, out, lse, scratch, kNoAllocScratchBytes, stream);
+}
+
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
                               cudaStream_t stream) {
   if (a == nullptr || b == nullptr || d == nullptr) return DSA_ERR_INVALID_ARG;
