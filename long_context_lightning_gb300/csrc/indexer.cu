@@ -59,14 +59,23 @@ struct IdxParams {
   int* err;
 };
 
-// Work item -> group, by binary search over the group prefix (monotone).
-__device__ __forceinline__ int find_group(const int32_t* start, int n_groups, int item) {
-  int lo = 0, hi = n_groups - 1;  // last g with start[g] <= item
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(start + mid) <= item) lo = mid; else hi = mid - 1;
+// Work item -> group: the last g with start[g] <= item (start is non-decreasing,
+// start[0] = 0).  One warp narrows the range 32-fold per round of loads.
+__device__ __forceinline__ int find_group_warp(const int32_t* start, int n_groups, int item) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n_groups - 1;
+  while (hi - lo > 31) {
+    const int q = lo + (int)((int64_t)(hi - lo) * lane / 31);
+    const unsigned m = __ballot_sync(0xffffffffu, __ldg(start + q) <= item);
+    const int last = 31 - __clz(m);  // lane 0 probes lo, which always qualifies
+    const int nlo = __shfl_sync(0xffffffffu, q, last);
+    const int nhi = last < 31 ? __shfl_sync(0xffffffffu, q, min(last + 1, 31)) - 1 : hi;
+    lo = nlo;
+    hi = max(nhi, nlo);
   }
-  return lo;
+  const int q = lo + lane;
+  const unsigned m = __ballot_sync(0xffffffffu, q <= hi && __ldg(start + q) <= item);
+  return lo + (31 - __clz(m));
 }
 
 template <int KB, int NH, int G>
@@ -81,6 +90,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* first_group = reinterpret_cast<int*>(smem + C::OFF_MISC + 8);
 
   auto bar_a_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_a_empty = [&](int s) { return smem_u32(bars + C::STAGES + s); };
@@ -113,25 +123,32 @@ __global__ void __launch_bounds__(192, 1)
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  pdl_wait();     // the plan (previous grid) is complete and visible from here on
+  pdl_trigger();
 
-  // this block's contiguous range of work items
+  // this block's contiguous range of work items and the group of its first one
   const int n_groups = p.plan.header[0];
   const int total = p.plan.header[1];
   const int64_t nb = gridDim.x;
   const int w0 = (int)((int64_t)total * blockIdx.x / nb);
   const int w1 = (int)((int64_t)total * (blockIdx.x + 1) / nb);
   const int32_t* gstart = p.plan.g_tile_start;
+  if (warp == 0) {
+    const int g = (w0 < w1) ? find_group_warp(gstart, n_groups, w0) : 0;
+    if (lane == 0) first_group[0] = g;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int g_first = first_group[0];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && w0 < w1) {
       int stage = 0;
       uint32_t phase = 0;
-      int g = find_group(gstart, n_groups, w0);
+      int g = g_first;
       int g_next = __ldg(gstart + g + 1);
       int b_loads = 0;
       int4 gi = p.plan.g_info[g];
@@ -200,7 +217,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      int g = find_group(gstart, n_groups, w0);
+      int g = g_first;
       int g_next = __ldg(gstart + g + 1);
       int b_uses = 0;
       for (int item = w0; item < w1; ++item) {
@@ -248,7 +265,7 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool bad = (w0 >= w1);
-    int g = bad ? 0 : find_group(gstart, n_groups, w0);
+    int g = g_first;
     int g_next = bad ? 0 : __ldg(gstart + g + 1);
     int4 gi = make_int4(0, 0, 0, 0);
     int qn[G];
@@ -340,8 +357,15 @@ cudaError_t launch_t(const IndexerLaunch& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   // Upper bound of work items: every query group scans at most ceil(max_n/128)
   // tiles.  The grid is one block per SM; blocks with an empty range exit.
-  indexer_kernel<KB, NH, G><<<a.num_sms, C::THREADS, C::SMEM_BYTES, stream>>>(tm_k, tm_q, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_sms, 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at = pdl_attribute();
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, indexer_kernel<KB, NH, G>, tm_k, tm_q, p);
 }
 
 }  // namespace

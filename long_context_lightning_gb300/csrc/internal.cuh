@@ -92,6 +92,8 @@ constexpr int kIdxTileKeys = 128;  // keys per indexer work item (tcgen05 M)
 
 // Host launchers (each .cu file defines its own).
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream);
+// Launch attribute for programmatic dependent launch (kernels call pdl_wait()).
+cudaLaunchAttribute pdl_attribute();
 
 struct IndexerLaunch {
   CacheView k;

@@ -1,7 +1,8 @@
 // plan.cu -- per-call plan of a ragged batch: sequence and causal length of
 // every query token, and the indexer's flat list of (query group, 128-key
 // tile) work items.  One block; runs ahead of the compute kernels on the same
-// stream, so no host round trip is needed to size ragged work.
+// stream, so no host round trip is needed to size ragged work.  The batch's
+// two length arrays are staged in shared memory so every search is on-chip.
 #include "internal.cuh"
 
 namespace dsa {
@@ -9,7 +10,7 @@ namespace dsa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kMaxSeqs = 16384;  // sequence offsets kept in shared memory
+constexpr int kMaxSeqs = 16384;  // cu_seqlens, lengths and group offsets kept in shared memory
 
 // Exclusive block-wide scan of one int per thread; returns the prefix and
 // writes the block total to *total.  All threads of the block must call it.
@@ -39,9 +40,14 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return before;
 }
 
-__device__ __forceinline__ bool seq_ok(const PlanParams& p, int b, int* nq_out, int* len_out) {
-  const int c0 = __ldg(p.cu_seqlens_q + b), c1 = __ldg(p.cu_seqlens_q + b + 1);
-  const int len = __ldg(p.seq_lens_k + b);
+struct SeqArrays {
+  const int* cu;   // [B + 1]
+  const int* len;  // [B]
+};
+
+__device__ __forceinline__ bool seq_ok(const PlanParams& p, const SeqArrays& s, int b, int* nq_out, int* len_out) {
+  const int c0 = s.cu[b], c1 = s.cu[b + 1];
+  const int len = s.len[b];
   const int nq = c1 - c0;
   *nq_out = nq;
   *len_out = len;
@@ -49,10 +55,20 @@ __device__ __forceinline__ bool seq_ok(const PlanParams& p, int b, int* nq_out, 
 }
 
 __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
-  extern __shared__ int goff[];  // [B + 1] group offsets of the sequences
+  extern __shared__ int sm_plan[];
+  int* cu_s = sm_plan;                // [B + 1]
+  int* len_s = sm_plan + p.B + 1;     // [B]
+  int* goff = len_s + p.B;            // [B + 1] group offsets of the sequences
   __shared__ int warp_sums[32];
-  __shared__ int s_total;
   const int G = p.group;
+  pdl_trigger();  // the indexer's prologue may start; it waits for this grid before reading the plan
+
+  for (int i = threadIdx.x; i <= p.B; i += kPlanThreads) {
+    cu_s[i] = __ldg(p.cu_seqlens_q + i);
+    if (i < p.B) len_s[i] = __ldg(p.seq_lens_k + i);
+  }
+  __syncthreads();
+  const SeqArrays sa{cu_s, len_s};
 
   // (1) groups per sequence, and their offsets
   int running = 0;
@@ -61,7 +77,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     int ng = 0;
     if (b < p.B) {
       int nq, len;
-      if (seq_ok(p, b, &nq, &len)) {
+      if (seq_ok(p, sa, b, &nq, &len)) {
         ng = (nq + G - 1) / G;
       } else {
         atomicOr(p.err, DEV_ERR_BAD_INDEX);
@@ -81,11 +97,11 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     int lo = 0, hi = p.B - 1;  // last b with cu[b] <= t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.cu_seqlens_q + mid) <= t) lo = mid; else hi = mid - 1;
+      if (cu_s[mid] <= t) lo = mid; else hi = mid - 1;
     }
     int nq, len;
-    const bool ok = seq_ok(p, lo, &nq, &len);
-    const int i = t - __ldg(p.cu_seqlens_q + lo);
+    const bool ok = seq_ok(p, sa, lo, &nq, &len);
+    const int i = t - cu_s[lo];
     p.plan.q_seq[t] = lo;
     p.plan.q_n[t] = (ok && i >= 0 && i < nq) ? (len - nq + i + 1) : 0;
   }
@@ -104,8 +120,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       const int b = lo;
       const int j = g - goff[b];
       int nq, len;
-      seq_ok(p, b, &nq, &len);
-      const int q0 = __ldg(p.cu_seqlens_q + b) + j * G;
+      seq_ok(p, sa, b, &nq, &len);
+      const int q0 = cu_s[b] + j * G;
       const int cnt = min(G, nq - j * G);
       const int n_last = len - nq + j * G + cnt;  // causal n of the group's last query
       p.plan.g_info[g] = make_int4(b, q0, cnt, n_last);
@@ -127,13 +143,23 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
   if (p.B > kMaxSeqs) return cudaErrorInvalidValue;
-  const size_t smem = sizeof(int) * (size_t)(p.B + 1);
+  const size_t smem = sizeof(int) * (size_t)(3 * p.B + 2);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   plan_kernel<<<1, kPlanThreads, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while its predecessor on the stream still runs, and must call pdl_wait()
+// before it reads anything the predecessor writes.
+cudaLaunchAttribute pdl_attribute() {
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  return at;
 }
 
 }  // namespace dsa

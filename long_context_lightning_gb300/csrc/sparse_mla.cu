@@ -15,22 +15,29 @@
 //   O^T[v, h]  += C[key, v]^T . P^T[key, h] M = 128 value dims per block, N = 64
 //                 heads, K = 128 keys (C block read MN-major, P MN-major)
 // so the 64-head MQA tile is a real dense contraction with every TMEM lane in
-// use (O^T: 4 x 64 columns, S^T: 64 columns).  One thread owns one key of S^T:
-// the per-head softmax max over the 128 keys is a 62-shuffle transpose
-// reduction per warp plus a 4-warp exchange; the running max is only raised
-// when a head's max grows by more than 2^8 (the exact result is unchanged,
-// only the reference point moves), so O^T is rarely rescaled in TMEM.
+// use (O^T: 4 x 64 columns, S^T: 64 columns).  One thread owns one key of S^T
+// for 32 heads: the per-head softmax max over the 128 keys is a 31-shuffle
+// transpose reduction per warp plus a 4-quadrant exchange; the running max is
+// only raised when a head's max grows by more than 2^8 (the exact result is
+// unchanged, only the reference point moves), so O^T is rarely rescaled.
+//
+// Row gather: for the 576-dim latent, TMA tile::gather4 moves four selected
+// rows x 64 dims per instruction straight into the swizzled block, all nine
+// blocks of a tile in flight at once, completion counted in bytes on one
+// mbarrier per block.  (The 80-dim test latent uses 16-byte cp.async copies.)
 //
 // Split over a cluster: the selected rows of one query are divided among the
 // blocks of a thread-block cluster; each block keeps its partial (m, l, O) and
 // the cluster combines them through distributed shared memory, so partial
 // outputs never travel through global memory.
 //
-// Warp roles (288 threads, one block per SM):
-//   warps 0..3  row gather: index -> pool row (paged or contiguous), 16-byte
-//               cp.async copies into the swizzled blocks, one barrier per block
-//   warp 4      TMEM owner, query TMA, MMA issuer (one thread)
-//   warps 5..8  softmax (one per TMEM lane quadrant), then the combine
+// Warp roles (416 threads, one block per SM):
+//   warps 0..3   row gather (index -> pool row, paged or contiguous)
+//   warp 4       TMEM owner, query TMA, MMA issuer (one thread)
+//   warps 5..12  softmax: two warps per TMEM lane quadrant, 32 heads each;
+//                then the combine
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace dsa {
@@ -39,23 +46,25 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // raise the running max only past 2^8
+constexpr int kSoftmaxThreads = 256;
 
-template <int NB, int MB, bool PSEP>
+template <int NB, int MB, bool PSEP, bool TMA4>
 struct MlaCfg {
-  static constexpr int THREADS = 288;
+  static constexpr int THREADS = 160 + kSoftmaxThreads;
   static constexpr int BLK = 128 * 128;               // one [128 rows x 64 dims] block
   static constexpr int OFF_Q = 0;                     // NB x [64 heads x 64 dims]
   static constexpr int OFF_KV = OFF_Q + NB * 64 * 128;
   static constexpr int OFF_P = PSEP ? OFF_KV + NB * BLK : OFF_KV + (NB - 1) * BLK;
-  static constexpr int OFF_ROWS = (PSEP ? OFF_P + BLK : OFF_KV + NB * BLK);  // 2 x 128 row pointers
-  static constexpr int OFF_VALID = OFF_ROWS + 2 * 128 * 8;                   // 2 x 128 int
+  static constexpr int OFF_ROWS = (PSEP ? OFF_P + BLK : OFF_KV + NB * BLK);  // 2 x 128 row pointers (cp.async)
+  static constexpr int ROWS_BYTES = TMA4 ? 0 : 2 * 128 * 8;
+  static constexpr int OFF_VALID = OFF_ROWS + ROWS_BYTES;                    // 2 x 128 int
   static constexpr int OFF_RED = OFF_VALID + 2 * 128 * 4;                    // 4 x 64 float
   static constexpr int OFF_MRUN = OFF_RED + 4 * 64 * 4;                      // 64 float
   static constexpr int OFF_ALPHA = OFF_MRUN + 64 * 4;                        // 64 float
   static constexpr int OFF_ML = OFF_ALPHA + 64 * 4;                          // 2 x 64 float (m, l)
   static constexpr int OFF_F = OFF_ML + 2 * 64 * 4;                          // 64 float
   static constexpr int OFF_BAR = OFF_F + 64 * 4;
-  static constexpr int N_BARS = 2 * NB + 5;
+  static constexpr int N_BARS = 2 * NB + 7;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = (MB * 64 + 64) <= 128 ? 128 : (MB * 64 + 64) <= 256 ? 256 : 512;
@@ -89,12 +98,43 @@ __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
   return r != 0;
 }
 
-template <int NB, int MB, bool PSEP>
-__global__ void __launch_bounds__(288, 1)
+// Per-lane reduction of 32 values across the warp by halving exchanges: lane l
+// ends with the reduction over all 32 lanes of element l.
+template <bool MAX>
+__device__ __forceinline__ float transpose_reduce32(const float (&x)[32], int lane) {
+  float y[16];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float keep = hi ? x[16 + i] : x[i];
+      const float send = hi ? x[i] : x[16 + i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, 16);
+      y[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+#pragma unroll
+  for (int w = 8, n = 8; w >= 1; w >>= 1, n >>= 1) {
+    const bool hi = lane & w;
+#pragma unroll
+    for (int i = 0; i < n; ++i) {
+      const float keep = hi ? y[n + i] : y[i];
+      const float send = hi ? y[i] : y[n + i];
+      const float got = __shfl_xor_sync(0xffffffffu, send, w);
+      y[i] = MAX ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  return y[0];
+}
+
+template <int NB, int MB, bool PSEP, bool TMA4>
+__global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
                       const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_q3,
+                      const __grid_constant__ CUtensorMap tm_c0, const __grid_constant__ CUtensorMap tm_c1,
+                      const __grid_constant__ CUtensorMap tm_c2, const __grid_constant__ CUtensorMap tm_c3,
                       MlaParams p) {
-  using C = MlaCfg<NB, MB, PSEP>;
+  using C = MlaCfg<NB, MB, PSEP, TMA4>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -117,6 +157,7 @@ __global__ void __launch_bounds__(288, 1)
   const uint32_t bar_q_full = smem_u32(bars + 2 * NB + 2);
   const uint32_t bar_o_done = smem_u32(bars + 2 * NB + 3);
   const uint32_t bar_drain = smem_u32(bars + 2 * NB + 4);
+  auto bar_valid = [&](int par) { return smem_u32(bars + 2 * NB + 5 + par); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
@@ -125,26 +166,23 @@ __global__ void __launch_bounds__(288, 1)
   const int li = blockIdx.y / p.T;
   const MlaLayerView& L = p.layer[li];
   const CUtensorMap* tm_q = li == 0 ? &tm_q0 : li == 1 ? &tm_q1 : li == 2 ? &tm_q2 : &tm_q3;
-
-  const int n_t = p.q_n[t];
-  const int b = p.q_seq[t];
-  const int nvalid = min(n_t, p.k);
-  const int tiles = (nvalid + 127) / 128;
-  const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
-  const int my_tiles = j1 - j0;
+  const CUtensorMap* tm_c = li == 0 ? &tm_c0 : li == 1 ? &tm_c1 : li == 2 ? &tm_c2 : &tm_c3;
 
   if (threadIdx.x == 0) {
     for (int kb = 0; kb < NB; ++kb) {
-      mbar_init(bar_full(kb), 128);
+      mbar_init(bar_full(kb), TMA4 ? 1 : 128);
       mbar_init(bar_empty(kb), 1);
     }
     mbar_init(bar_s_full, 1);
-    mbar_init(bar_p_full, 128);
+    mbar_init(bar_p_full, kSoftmaxThreads);
     mbar_init(bar_q_full, 1);
     mbar_init(bar_o_done, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(bar_valid(0), 128);
+    mbar_init(bar_valid(1), 128);
     *abort_flag = 0;
     fence_mbar_init();
+    if (TMA4) prefetch_tmap(tm_c);
   }
   if (threadIdx.x >= 160 && threadIdx.x < 224) mrun_s[threadIdx.x - 160] = -INFINITY;
   if (warp == 4) {
@@ -155,71 +193,102 @@ __global__ void __launch_bounds__(288, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the query is a caller input: its load may overlap the previous grid
+  if (warp == 4 && lane == 0) {
+    mbar_arrive_expect_tx(bar_q_full, NB * 64 * 128);
+    for (int kb = 0; kb < NB; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 64 * 128, tm_q, bar_q_full, kb * 64, 0, t);
+  }
+  pdl_wait();  // positions and plan of the previous grids are complete from here on
+  pdl_trigger();
+
+  const int n_t = p.q_n[t];
+  const int b = p.q_seq[t];
+  const int nvalid = min(n_t, p.k);
+  const int tiles = (nvalid + 127) / 128;
+  const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
+  const int my_tiles = j1 - j0;
 
   if (warp < 4) {
     // ---------------------------------------------------------- row gather
-    const int pt = threadIdx.x;              // 0..127
-    const int chunk = pt & 7;                // 16-byte chunk within a 128-byte row
+    const int pt = threadIdx.x;              // key of the tile this thread resolves
     const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
     bool bad = false;
     for (int jj = 0; jj < my_tiles; ++jj) {
       const int j = j0 + jj;
       const int par = jj & 1;
-      {  // row of key pt of this tile
+      const uint32_t phase = jj & 1;
+      int64_t row = -1;
+      {
         const int e = j * 128 + pt;
         int pos = e < nvalid ? __ldg(idx_row + e) : -1;
-        const __nv_bfloat16* src = nullptr;
         if (pos >= n_t || pos < -1) {
           atomicOr(p.err, DEV_ERR_BAD_INDEX);
           pos = -1;
         }
         if (pos >= 0) {
-          const int64_t r = cache_row(L.kv, b, pos);
-          if (r < 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
-          else src = L.kv.base + r * L.kv.row_stride;
+          row = cache_row(L.kv, b, pos);
+          if (row < 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
         }
-        rows_s[par * 128 + pt] = src;
-        valid_s[par * 128 + pt] = src != nullptr;
+        valid_s[par * 128 + pt] = row >= 0;
+        if (!TMA4) rows_s[par * 128 + pt] = row >= 0 ? L.kv.base + row * L.kv.row_stride : nullptr;
       }
-      named_bar_sync(2, 128);
-      const uint32_t phase = jj & 1;
+      mbar_arrive(bar_valid(par));
+      if constexpr (TMA4) {
+        // lanes 0..7 of warp w gather rows 32w + 4l .. +3; an unused slot reads
+        // pool row 0 (finite data; its probability is zero)
+        const int32_t rr = row >= 0 ? (int32_t)row : 0;
+        const int src = (lane & 7) * 4;
+        const int32_t r0 = __shfl_sync(0xffffffffu, rr, src), r1 = __shfl_sync(0xffffffffu, rr, src + 1);
+        const int32_t r2 = __shfl_sync(0xffffffffu, rr, src + 2), r3 = __shfl_sync(0xffffffffu, rr, src + 3);
+        if (lane < 8) {
+          const uint32_t dst_off = (uint32_t)(warp * 8 + lane) * 512;
 #pragma unroll 1
-      for (int kb = 0; kb < NB; ++kb) {
-        bad |= !mbar_wait(bar_empty(kb), phase ^ 1, abort_flag, p.err);
-        if (!bad) {
-          const uint32_t dst0 = sbase + C::OFF_KV + kb * C::BLK;
-          const int col = kb * 64 + chunk * 8;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = (pt >> 3) + 16 * i;
-            const __nv_bfloat16* src = rows_s[par * 128 + r];
-            const bool ok = src != nullptr && col < p.d_qk;
-            cp_async_16(dst0 + r * 128 + ((chunk ^ (r & 7)) << 4), ok ? (const void*)(src + col) : (const void*)L.kv.base,
-                        ok ? 16u : 0u);
+          for (int kb = 0; kb < NB; ++kb) {
+            bad |= !mbar_wait(bar_empty(kb), phase ^ 1, abort_flag, p.err);
+            if (warp == 0 && lane == 0) mbar_arrive_expect_tx(bar_full(kb), C::BLK);
+            if (!bad)
+              tma_gather4(sbase + C::OFF_KV + kb * C::BLK + dst_off, tm_c, bar_full(kb), kb * 64, r0, r1, r2, r3);
           }
         }
-        cp_async_commit();
-        // signal the block issued two steps ago once its copies have landed
-        if (kb >= 2) {
-          cp_async_wait_group<2>();
-          fence_proxy_async_smem();
-          mbar_arrive(bar_full(kb - 2));
+        // lanes 8..31 wait here for the issuing lanes: nobody may rewrite this
+        // tile parity's valid flags before the empties of the next tile came back
+        __syncwarp();
+      } else {
+        named_bar_sync(2, 128);
+        const int chunk = pt & 7;
+#pragma unroll 1
+        for (int kb = 0; kb < NB; ++kb) {
+          bad |= !mbar_wait(bar_empty(kb), phase ^ 1, abort_flag, p.err);
+          if (!bad) {
+            const uint32_t dst0 = sbase + C::OFF_KV + kb * C::BLK;
+            const int col = kb * 64 + chunk * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = (pt >> 3) + 16 * i;
+              const __nv_bfloat16* src = rows_s[par * 128 + r];
+              const bool ok = src != nullptr && col < p.d_qk;
+              cp_async_16(dst0 + r * 128 + ((chunk ^ (r & 7)) << 4),
+                          ok ? (const void*)(src + col) : (const void*)L.kv.base, ok ? 16u : 0u);
+            }
+          }
+          cp_async_commit();
+          if (kb >= 2) {  // signal the block issued two steps ago once its copies have landed
+            cp_async_wait_group<2>();
+            fence_proxy_async_smem();
+            mbar_arrive(bar_full(kb - 2));
+          }
         }
+        cp_async_wait_group<0>();
+        fence_proxy_async_smem();
+        for (int kb = (NB >= 2 ? NB - 2 : 0); kb < NB; ++kb) mbar_arrive(bar_full(kb));
       }
-      cp_async_wait_group<0>();
-      fence_proxy_async_smem();
-      for (int kb = (NB >= 2 ? NB - 2 : 0); kb < NB; ++kb) mbar_arrive(bar_full(kb));
     }
-    cp_async_wait_all();
+    if (!TMA4) cp_async_wait_all();
   } else if (warp == 4) {
     // ---------------------------------------------- query TMA + MMA issuer
     if (lane == 0) {
-      bool bad = false;
-      if (my_tiles > 0) {
-        mbar_arrive_expect_tx(bar_q_full, NB * 64 * 128);
-        for (int kb = 0; kb < NB; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 64 * 128, tm_q, bar_q_full, kb * 64, 0, t);
-        bad = !mbar_wait(bar_q_full, 0, abort_flag, p.err);
-      }
+      bool bad = !mbar_wait(bar_q_full, 0, abort_flag, p.err);
+      if (bad) mbar_wait_drain(bar_q_full, 0);  // the query copy lands before the block may exit
       constexpr uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
       constexpr uint32_t idesc_o = mma_idesc_bf16(128, 64, true, true);
       for (int jj = 0; jj < my_tiles && !bad; ++jj) {
@@ -261,55 +330,33 @@ __global__ void __launch_bounds__(288, 1)
   } else {
     // ------------------------------------------------------------- softmax
     const int quad = warp & 3;
+    const int half = (warp - 5) >> 2;        // heads 32*half .. +31
     const int row = quad * 32 + lane;        // key (S^T) or value dim (O^T) lane
-    const int st = threadIdx.x - 160;        // 0..127
+    const int st = threadIdx.x - 160;        // 0..255
+    const int h0 = half * 32;
     const float c = L.scale * kLog2e;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    float lsum[64];
+    float lsum[32];
 #pragma unroll
-    for (int h = 0; h < 64; ++h) lsum[h] = 0.f;
+    for (int i = 0; i < 32; ++i) lsum[i] = 0.f;
     bool bad = false;
     for (int jj = 0; jj < my_tiles; ++jj) {
       const int par = jj & 1;
+      bad |= !mbar_wait(bar_valid(par), (jj >> 1) & 1, abort_flag, p.err);
+      const bool kv = valid_s[par * 128 + row] != 0;
       bad |= !mbar_wait(bar_s_full, par, abort_flag, p.err);
       tc_fence_after();
-      float x[64];
-#pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
-        uint32_t r[16];
-        tmem_ld16(lane_base + C::S_COL + c16 * 16, r);
+      float x[32];
+      {
+        uint32_t r[32];
+        tmem_ld32(lane_base + C::S_COL + h0, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) x[c16 * 16 + j] = __uint_as_float(r[j]);
+        for (int i = 0; i < 32; ++i) x[i] = kv ? __uint_as_float(r[i]) * c : -INFINITY;
       }
-      const bool kv = valid_s[par * 128 + row] != 0;
-#pragma unroll
-      for (int h = 0; h < 64; ++h) x[h] = kv ? x[h] * c : -INFINITY;
-      // per-head max over this warp's 32 keys: transpose reduction, lane l ends
-      // with heads 2l and 2l+1
-      float y[32];
-      {
-        const bool hi = lane & 16;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float keep = hi ? x[32 + i] : x[i];
-          const float send = hi ? x[i] : x[32 + i];
-          y[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-        }
-      }
-#pragma unroll
-      for (int w = 8, n = 16; w >= 1; w >>= 1, n >>= 1) {
-        const bool hi = lane & w;
-#pragma unroll
-        for (int i = 0; i < n; ++i) {
-          const float keep = hi ? y[n + i] : y[i];
-          const float send = hi ? y[i] : y[n + i];
-          y[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
-        }
-      }
-      red_s[quad * 64 + 2 * lane] = y[0];
-      red_s[quad * 64 + 2 * lane + 1] = y[1];
-      named_bar_sync(3, 128);
+      // per-head max over this warp's 32 keys; lane l ends with head h0 + l
+      red_s[quad * 64 + h0 + lane] = transpose_reduce32<true>(x, lane);
+      named_bar_sync(3, kSoftmaxThreads);
       bool rescale = false;
       if (st < 64) {
         const float mt = fmaxf(fmaxf(red_s[st], red_s[64 + st]), fmaxf(red_s[128 + st], red_s[192 + st]));
@@ -322,70 +369,45 @@ __global__ void __launch_bounds__(288, 1)
         }
         alpha_s[st] = alpha;
       }
-      rescale = bar_red_or(4, 128, rescale);
-      // probabilities, running sums, P^T row (this key's 64 heads, bf16)
+      rescale = bar_red_or(4, kSoftmaxThreads, rescale);
+      // probabilities, running sums, this key's P^T row for heads h0..h0+31 (bf16)
       const uint32_t prow = sbase + C::OFF_P + row * 128;
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
+      for (int cc = 0; cc < 4; ++cc) {
         float pv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int h = cc * 8 + j;
-          pv[j] = x[h] == -INFINITY ? 0.f : exp2f(x[h] - mrun_s[h]);  // no valid key yet: m is -inf too
-          lsum[h] = fmaf(lsum[h], alpha_s[h], pv[j]);
+          const int i = cc * 8 + j;
+          pv[j] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - mrun_s[h0 + i]);  // no valid key yet: m is -inf too
+          lsum[i] = fmaf(lsum[i], alpha_s[h0 + i], pv[j]);
         }
-        st_shared_v4(prow + ((cc ^ (row & 7)) << 4), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
+        const int chunk = half * 4 + cc;
+        st_shared_v4(prow + ((chunk ^ (row & 7)) << 4), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
                      pack_bf16x2(pv[4], pv[5]), pack_bf16x2(pv[6], pv[7]));
       }
       fence_proxy_async_smem();
       if (rescale && !bad) {
         // move O^T to the new reference point: column h times alpha[h]
         for (int mb = 0; mb < MB; ++mb) {
+          uint32_t r[32];
+          tmem_ld32(lane_base + mb * 64 + h0, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c16 = 0; c16 < 4; ++c16) {
-            uint32_t r[16];
-            tmem_ld16(lane_base + mb * 64 + c16 * 16, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha_s[c16 * 16 + j]);
-            tmem_st16(lane_base + mb * 64 + c16 * 16, r);
-          }
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha_s[h0 + i]);
+          tmem_st32(lane_base + mb * 64 + h0, r);
         }
         tmem_wait_st();
       }
       tc_fence_before();
       mbar_arrive(bar_p_full);
-      named_bar_sync(3, 128);  // alpha_s / mrun_s are rewritten by the next tile
+      named_bar_sync(3, kSoftmaxThreads);  // alpha_s / mrun_s / red_s are rewritten by the next tile
     }
-    // l per head over this block's keys: transpose reduction of the lane sums
-    {
-      float y[32];
-      {
-        const bool hi = lane & 16;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float keep = hi ? lsum[32 + i] : lsum[i];
-          const float send = hi ? lsum[i] : lsum[32 + i];
-          y[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-        }
-      }
-#pragma unroll
-      for (int w = 8, n = 16; w >= 1; w >>= 1, n >>= 1) {
-        const bool hi = lane & w;
-#pragma unroll
-        for (int i = 0; i < n; ++i) {
-          const float keep = hi ? y[n + i] : y[i];
-          const float send = hi ? y[i] : y[n + i];
-          y[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
-        }
-      }
-      red_s[quad * 64 + 2 * lane] = y[0];
-      red_s[quad * 64 + 2 * lane + 1] = y[1];
-      named_bar_sync(3, 128);
-      if (st < 64) {
-        ml_s[st] = mrun_s[st];
-        ml_s[64 + st] = red_s[st] + red_s[64 + st] + red_s[128 + st] + red_s[192 + st];
-      }
+    // l per head over this block's keys
+    red_s[quad * 64 + h0 + lane] = transpose_reduce32<false>(lsum, lane);
+    named_bar_sync(3, kSoftmaxThreads);
+    if (st < 64) {
+      ml_s[st] = mrun_s[st];
+      ml_s[64 + st] = red_s[st] + red_s[64 + st] + red_s[128 + st] + red_s[192 + st];
     }
     if (my_tiles > 0) bad |= !mbar_wait(bar_o_done, 0, abort_flag, p.err);
     tc_fence_after();
@@ -413,23 +435,21 @@ __global__ void __launch_bounds__(288, 1)
   __syncthreads();
   if (warp >= 5) {
     const int quad = warp & 3;
+    const int h0 = ((warp - 5) >> 2) * 32;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     for (int mb = 0; mb < MB; ++mb) {
       const int v = mb * 128 + row;
+      uint32_t r[32];
+      if (my_tiles > 0) {
+        tmem_ld32(lane_base + mb * 64 + h0, r);
+        tmem_wait_ld();
+      }
+      if (v < p.d_v) {
 #pragma unroll
-      for (int c16 = 0; c16 < 4; ++c16) {
-        uint32_t r[16];
-        if (my_tiles > 0) {
-          tmem_ld16(lane_base + mb * 64 + c16 * 16, r);
-          tmem_wait_ld();
-        }
-        if (v < p.d_v) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int h = c16 * 16 + j;
-            obuf[h * p.d_v + v] = my_tiles > 0 ? __uint_as_float(r[j]) * f_s[h] : 0.f;
-          }
+        for (int j = 0; j < 32; ++j) {
+          const int h = h0 + j;
+          obuf[h * p.d_v + v] = my_tiles > 0 ? __uint_as_float(r[j]) * f_s[h] : 0.f;
         }
       }
     }
@@ -467,19 +487,32 @@ __global__ void __launch_bounds__(288, 1)
 
 int g_max_cluster_mla[2] = {0, 0};
 
-template <int NB, int MB, bool PSEP>
+template <int NB, int MB, bool PSEP, bool TMA4>
 cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
-  using C = MlaCfg<NB, MB, PSEP>;
-  auto kern = sparse_mla_kernel<NB, MB, PSEP>;
-  CUtensorMap tm[DSA_MAX_LAYERS];
+  using C = MlaCfg<NB, MB, PSEP, TMA4>;
+  auto kern = sparse_mla_kernel<NB, MB, PSEP, TMA4>;
+  CUtensorMap tq[DSA_MAX_LAYERS], tc[DSA_MAX_LAYERS];
   for (int l = 0; l < DSA_MAX_LAYERS; ++l) {
     const int ls = l < a.n_layers ? l : 0;
-    const uint64_t dims[3] = {(uint64_t)a.d_qk, (uint64_t)a.layer[ls].H, (uint64_t)a.T};
-    const uint64_t strides[2] = {(uint64_t)a.d_qk * 2, (uint64_t)a.d_qk * a.layer[ls].H * 2};
-    const uint32_t box[3] = {64u, 64u, 1u};
-    if (encode_tmap(&tm[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.layer[ls].q, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    const MlaLayerView& lv = a.layer[ls];
+    {
+      const uint64_t dims[3] = {(uint64_t)a.d_qk, (uint64_t)lv.H, (uint64_t)a.T};
+      const uint64_t strides[2] = {(uint64_t)a.d_qk * 2, (uint64_t)a.d_qk * lv.H * 2};
+      const uint32_t box[3] = {64u, 64u, 1u};
+      if (encode_tmap(&tq[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, lv.q, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    if (TMA4) {
+      const uint64_t dims[2] = {(uint64_t)a.d_qk, (uint64_t)lv.kv.num_rows};
+      const uint64_t strides[1] = {(uint64_t)lv.kv.row_stride * 2};
+      const uint32_t box[2] = {64u, 1u};
+      if (encode_tmap(&tc[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lv.kv.base, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    } else {
+      tc[l] = tq[l];  // unused by the cp.async gather
+    }
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
@@ -526,22 +559,23 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute at;
-  at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = c;
-  at.val.clusterDim.y = 1;
-  at.val.clusterDim.z = 1;
-  cfg.attrs = &at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tm[0], tm[1], tm[2], tm[3], p);
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = c;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1] = pdl_attribute();
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, tq[0], tq[1], tq[2], tq[3], tc[0], tc[1], tc[2], tc[3], p);
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  if (a.d_qk == 576 && a.d_v == 512) return launch_t<9, 4, false>(a, stream, 0);
-  if (a.d_qk == 80 && a.d_v == 64) return launch_t<2, 1, true>(a, stream, 1);
+  if (a.d_qk == 576 && a.d_v == 512) return launch_t<9, 4, false, true>(a, stream, 0);
+  if (a.d_qk == 80 && a.d_v == 64) return launch_t<2, 1, true, false>(a, stream, 1);
   return cudaErrorInvalidValue;
 }
 

@@ -3,22 +3,25 @@
 // "How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works / Model:
 // the top-2048 past tokens are kept and a context below that is taken whole.
 //
-// One thread-block cluster per query row; block c of the cluster owns a
-// contiguous chunk of the row.  Scores become order-preserving 32-bit keys
-// (-0.0 folded onto +0.0) and a three-digit radix select (11 + 11 + 10 bits)
-// finds the k-th largest key: each digit is a shared-memory histogram per
-// block, summed across the cluster through distributed shared memory, so the
-// row is never re-partitioned through global memory.  Each block then knows
-// how many of its keys are above the threshold and how many equal it; equal
-// keys are granted to the lowest positions first, and an ordered block scan
-// writes the selected positions in ascending order.  When the chunk fits in
-// shared memory the row is read from global memory exactly once.
+// One thread-block cluster per query row (one block when the row fits); block
+// c of the cluster owns a contiguous chunk of the row.  Scores become
+// order-preserving 32-bit keys (-0.0 folded onto +0.0) and a three-digit radix
+// select (11 + 11 + 10 bits) finds the k-th largest key: each digit is a
+// shared-memory histogram per block (lanes of a warp that hit the same bin are
+// merged with match.any before one atomic), summed across the cluster through
+// distributed shared memory.  Each block then knows how many of its keys are
+// above the threshold and how many equal it; equal keys are granted to the
+// lowest positions first.  The ordered write is per warp: each warp owns a
+// contiguous range of the chunk and places its selections with ballots, after
+// one 32-entry scan of the warps' counts.  When the chunk fits in shared
+// memory the row is read from global memory exactly once.
 #include "internal.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMaxCacheKeys = 45056;  // 176 KB of cached keys per block
 
@@ -52,19 +55,42 @@ __device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
   if (lane == 31) wsum[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = lane < kThreads / 32 ? wsum[lane] : 0;
+    int s = wsum[lane];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, s, o);
       if (lane >= o) s += y;
     }
-    if (lane < kThreads / 32) wsum[lane] = s;
+    wsum[lane] = s;
   }
   __syncthreads();
   const int r = (warp ? wsum[warp - 1] : 0) + x - v;
-  *total = wsum[kThreads / 32 - 1];
+  *total = wsum[kWarps - 1];
   __syncthreads();
   return r;
+}
+
+__device__ __forceinline__ int warp_excl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  return x - v;
+}
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Every lane of the warp calls this with the same control flow.
+__device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active) {
+  const unsigned m = __match_any_sync(0xffffffffu, active ? bin : 0xffffffffu);
+  if (active && (threadIdx.x & 31) == (unsigned)(__ffs(m) - 1)) atomicAdd(&h[bin], (uint32_t)__popc(m));
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
@@ -73,14 +99,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   uint32_t* tot = sm + 3 * kBins;         // [kBins] cluster-summed histogram of the current digit
   uint32_t* cache = sm + 4 * kBins;       // [cache_keys]
   __shared__ int wsum[32];
+  __shared__ int w_gt[kWarps], w_eq[kWarps], w_eqb[kWarps], w_selb[kWarps];
   __shared__ uint32_t s_digit, s_rem, s_local_above;
   __shared__ uint32_t s_xch[2];           // this block's (keys above threshold, keys equal to it)
 
   const int t = blockIdx.y;
   const uint32_t crank = cluster_ctarank();
   const uint32_t csize = cluster_nctarank();
+  pdl_wait();  // scores and plan of the previous grids are complete from here on
+  pdl_trigger();
   const int n = p.q_n[t];
   const int k = p.k;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int32_t* out = p.idx + (int64_t)t * p.ld_idx;
 
   if (n <= k) {  // dense row (or a malformed one, n = 0): positions 0..n-1, then -1
@@ -101,52 +131,56 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   uint32_t prefix = 0;   // digits fixed so far
   uint32_t rem = k;      // how many keys still to take at/below the current prefix
   uint32_t local_greater = 0;
-  const int shifts[3] = {21, 10, 0};
-  const uint32_t masks[3] = {0x7FFu, 0x7FFu, 0x3FFu};
 
+#pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
-    const int sh = shifts[pass];
-    const uint32_t msk = masks[pass];
+    const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const int bits = pass == 2 ? 10 : 11;
+    const uint32_t msk = (1u << bits) - 1u;
+    const int psh = sh + bits;  // bits above this digit
     uint32_t* h = hist + pass * kBins;
-    const int psh = sh + (pass == 0 ? 11 : (pass == 1 ? 11 : 10));  // bits above this digit
     // ---- histogram of this digit over keys matching the prefix
     if (pass == 0) {
-      for (int i = threadIdx.x * 4; i < len; i += kThreads * 4) {
+      for (int i0 = 0; i0 < len; i0 += kThreads * 4) {
+        const int i = i0 + threadIdx.x * 4;
         const int s = c0 + i;
-        float v[4];
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
         if (s + 3 < c1) {
           const float4 f = __ldg(reinterpret_cast<const float4*>(row + s));
           v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
         } else {
-          for (int j = 0; j < 4; ++j) v[j] = (s + j < c1) ? row[s + j] : 0.f;
+          for (int j = 0; j < 4; ++j) if (s + j < c1) v[j] = row[s + j];
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          if (s + j >= c1) break;
+          const bool in = s + j < c1;
           const uint32_t key = ordered_key(v[j]);
-          if (cached) cache[i + j] = key;
-          atomicAdd(&h[key >> sh], 1u);
+          if (cached && in) cache[i + j] = key;
+          hist_add(h, key >> sh, in);
         }
       }
     } else {
-      for (int i = threadIdx.x; i < len; i += kThreads) {
-        const uint32_t key = cached ? cache[i] : ordered_key(row[c0 + i]);
-        if ((key >> psh) == prefix) atomicAdd(&h[(key >> sh) & msk], 1u);
+      for (int i0 = 0; i0 < len; i0 += kThreads) {
+        const int i = i0 + threadIdx.x;
+        const bool in = i < len;
+        const uint32_t key = in ? (cached ? cache[i] : ordered_key(row[c0 + i])) : 0u;
+        hist_add(h, (key >> sh) & msk, in && (key >> psh) == prefix);
       }
     }
     cluster_sync();  // every block's histogram of this digit is complete
     // ---- cluster-wide histogram
-    for (int bin = threadIdx.x; bin < kBins; bin += kThreads) {
-      uint32_t sum = 0;
+    const int nb = (int)msk + 1;
+    for (int bin = threadIdx.x; bin < nb; bin += kThreads) {
+      uint32_t sum = h[bin];
       const uint32_t local = smem_u32(h + bin);
-      for (uint32_t r = 0; r < csize; ++r) sum += (r == crank) ? h[bin] : ld_dsmem_u32(dsmem_addr(local, r));
+      for (uint32_t r = 0; r < csize; ++r)
+        if (r != crank) sum += ld_dsmem_u32(dsmem_addr(local, r));
       tot[bin] = sum;
     }
     __syncthreads();
     // ---- the digit holding the rem-th largest key: suffix sums from the top bin
     {
-      const int nb = (int)msk + 1;        // bins of this digit
-      const int per_t = (nb + kThreads - 1) / kThreads;  // 4 or 2
+      const int per_t = (nb + kThreads - 1) / kThreads;  // 2 or 1
       const int hi = nb - 1 - threadIdx.x * per_t;       // this thread's bins: hi, hi-1, ...
       int mine = 0;
       for (int j = 0; j < per_t; ++j) if (hi - j >= 0) mine += tot[hi - j];
@@ -155,23 +189,23 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
       for (int j = 0; j < per_t; ++j) {
         const int bin = hi - j;
         if (bin < 0) break;
-        const int c = tot[bin];
-        if ((uint32_t)above < rem && rem <= (uint32_t)(above + c)) {
+        const int cnt = tot[bin];
+        if ((uint32_t)above < rem && rem <= (uint32_t)(above + cnt)) {
           s_digit = bin;
           s_rem = rem - above;
         }
-        above += c;
+        above += cnt;
       }
       if (threadIdx.x == 0) s_local_above = 0;
       __syncthreads();
       const uint32_t d = s_digit;
-      // this block's own keys in bins above the chosen digit
-      uint32_t la = 0;
+      uint32_t la = 0;  // this block's own keys in bins above the chosen digit
       for (int bin = d + 1 + threadIdx.x; bin < nb; bin += kThreads) la += h[bin];
-      if (la) atomicAdd(&s_local_above, la);
+      la = warp_sum(la);
+      if (lane == 0 && la) atomicAdd(&s_local_above, la);
       __syncthreads();
       local_greater += s_local_above;
-      prefix = (prefix << (psh - sh)) | d;
+      prefix = (prefix << bits) | d;
       rem = s_rem;
       __syncthreads();
     }
@@ -192,43 +226,55 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     base += g + take_r;
     eq_before += e;
   }
-  const uint32_t take = min(local_equal, rem > eq_before ? rem - eq_before : 0u);
+  const int take = (int)min(local_equal, rem > eq_before ? rem - eq_before : 0u);
 
-  // ordered compaction: positions in ascending order
-  uint32_t eq_run = 0, sel_run = 0;
-  for (int i0 = 0; i0 < len; i0 += kThreads * 4) {
-    const int i = i0 + threadIdx.x * 4;
-    uint32_t key[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (i + j < len) key[j] = cached ? cache[i + j] : ordered_key(row[c0 + i + j]);
-      else key[j] = 0u;  // below every real key
+  // ---- ordered write: warp w owns the contiguous range [w0, w1) of the chunk
+  const int pw = ((len + kWarps - 1) / kWarps + 31) & ~31;
+  const int w0 = min(len, warp * pw), w1 = min(len, w0 + pw);
+  auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : ordered_key(row[c0 + i]); };
+  {
+    int gt = 0, eq = 0;
+    for (int i = w0 + lane; i < w1; i += 32) {
+      const uint32_t key = key_at(i);
+      gt += key > thr;
+      eq += key == thr;
     }
-    int n_eq = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) n_eq += (i + j < len && key[j] == thr);
-    int eq_tot;
-    int eq_rank = (int)eq_run + block_scan(n_eq, wsum, &eq_tot);
-    bool sel[4];
-    int n_sel = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool valid = i + j < len;
-      const bool eq = valid && key[j] == thr;
-      sel[j] = valid && (key[j] > thr || (eq && (uint32_t)eq_rank < take));
-      if (eq) ++eq_rank;
-      n_sel += sel[j];
+    gt = warp_sum(gt);
+    eq = warp_sum(eq);
+    if (lane == 0) {
+      w_gt[warp] = gt;
+      w_eq[warp] = eq;
     }
-    int sel_tot;
-    int pos = (int)(base + sel_run) + block_scan(n_sel, wsum, &sel_tot);
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (sel[j]) {
-        if (pos < k) out[pos] = c0 + i + j;
-        ++pos;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int e = w_eq[lane];
+    const int eb = warp_excl_scan(e);
+    const int tk = max(0, min(e, take - eb));
+    const int sb = warp_excl_scan(w_gt[lane] + tk);
+    w_eqb[lane] = eb;
+    w_selb[lane] = sb;
+  }
+  __syncthreads();
+  {
+    int eq_run = w_eqb[warp];
+    int pos_run = (int)base + w_selb[warp];
+    const unsigned lt = (1u << lane) - 1u;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+      const int i = i0 + lane;
+      const bool in = i < w1;
+      const uint32_t key = in ? key_at(i) : 0u;
+      const bool eqf = in && key == thr;
+      const unsigned eqm = __ballot_sync(0xffffffffu, eqf);
+      const bool sel = in && (key > thr || (eqf && eq_run + __popc(eqm & lt) < take));
+      const unsigned selm = __ballot_sync(0xffffffffu, sel);
+      if (sel) {
+        const int pos = pos_run + __popc(selm & lt);
+        if (pos < k) out[pos] = c0 + i;
       }
-    eq_run += eq_tot;
-    sel_run += sel_tot;
+      eq_run += __popc(eqm);
+      pos_run += __popc(selm);
+    }
   }
   cluster_sync();  // peers may still read this block's shared memory
 }
@@ -239,11 +285,6 @@ int g_max_cluster = 0;  // largest cluster size the device schedules for this ke
 
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  // cluster size: enough blocks to fill the GPU on few rows, and chunks that
-  // fit the shared-memory key cache when possible
-  int c = 1;
-  while (c < 16 && (int64_t)a.T * c * 2 <= a.num_sms) c *= 2;
-  while (c < 16 && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
   if (g_max_cluster == 0) {
     cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -266,7 +307,11 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
       g_max_cluster = 16;
     cudaGetLastError();
   }
-  if (c > g_max_cluster) c = g_max_cluster;
+  // cluster size: one block per row while rows fit its key cache and the rows
+  // alone give a few waves of blocks; more blocks per row for few long rows
+  int c = 1;
+  while (c < g_max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
+  while (c < g_max_cluster && (int64_t)a.T * c * 4 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 8192) c *= 2;
   const int per = (((a.max_n + c - 1) / c) + 3) & ~3;
   const int cache_keys = per <= kMaxCacheKeys ? per : 0;
   const size_t smem = (size_t)(4 * kBins + cache_keys) * 4;
@@ -289,13 +334,14 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute at;
-  at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = c;
-  at.val.clusterDim.y = 1;
-  at.val.clusterDim.z = 1;
-  cfg.attrs = &at;
-  cfg.numAttrs = 1;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = c;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1] = pdl_attribute();
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, topk_kernel, p);
 }
 
