@@ -31,17 +31,20 @@ struct IdxCfg {
   static constexpr int N = NH * G;                   // MMA N: (query, head) pairs
   static constexpr int A_BYTES = KB * 128 * 128;     // 128 keys x KB blocks of 64 dims
   static constexpr int B_BYTES = KB * N * 128;
+  // two query buffers when they are small, so the next group's queries load
+  // while the current group's last MMAs still read theirs
+  static constexpr int BSLOTS = (G == 1) ? 2 : 1;
   static constexpr int SMEM_BUDGET = 220 * 1024;
-  static constexpr int STAGES_FIT = (SMEM_BUDGET - B_BYTES - 4096) / A_BYTES;
+  static constexpr int STAGES_FIT = (SMEM_BUDGET - BSLOTS * B_BYTES - 4096) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
   static constexpr int THREADS = 192;
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-  static constexpr int OFF_W = OFF_B + B_BYTES;                 // fp32 [G][NH]
+  static constexpr int OFF_W = OFF_B + BSLOTS * B_BYTES;        // fp32 [G][NH]
   static constexpr int OFF_BAR = OFF_W + G * NH * 4;
-  static constexpr int N_BARS = 2 * STAGES + 2 + 4 + 1;
+  static constexpr int N_BARS = 2 * STAGES + 2 * BSLOTS + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;         // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;       // + alignment slack
   static_assert(N % 16 == 0 && N >= 16 && N <= 256, "tcgen05 M=128 needs N in [16, 256], multiple of 16");
@@ -94,11 +97,12 @@ __global__ void __launch_bounds__(192, 1)
 
   auto bar_a_full = [&](int s) { return smem_u32(bars + s); };
   auto bar_a_empty = [&](int s) { return smem_u32(bars + C::STAGES + s); };
-  const uint32_t bar_b_full = smem_u32(bars + 2 * C::STAGES);
-  const uint32_t bar_b_empty = smem_u32(bars + 2 * C::STAGES + 1);
-  auto bar_acc_full = [&](int a) { return smem_u32(bars + 2 * C::STAGES + 2 + a); };
-  auto bar_acc_empty = [&](int a) { return smem_u32(bars + 2 * C::STAGES + 4 + a); };
-  const uint32_t bar_drain = smem_u32(bars + 2 * C::STAGES + 6);
+  auto bar_b_full = [&](int u) { return smem_u32(bars + 2 * C::STAGES + u); };
+  auto bar_b_empty = [&](int u) { return smem_u32(bars + 2 * C::STAGES + C::BSLOTS + u); };
+  constexpr int kAccBar = 2 * C::STAGES + 2 * C::BSLOTS;
+  auto bar_acc_full = [&](int a) { return smem_u32(bars + kAccBar + a); };
+  auto bar_acc_empty = [&](int a) { return smem_u32(bars + kAccBar + 2 + a); };
+  const uint32_t bar_drain = smem_u32(bars + kAccBar + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -107,8 +111,10 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(bar_a_full(s), 1);
       mbar_init(bar_a_empty(s), 1);
     }
-    mbar_init(bar_b_full, 1);
-    mbar_init(bar_b_empty, 1);
+    for (int u = 0; u < C::BSLOTS; ++u) {
+      mbar_init(bar_b_full(u), 1);
+      mbar_init(bar_b_empty(u), 1);
+    }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_acc_full(a), 1);
       mbar_init(bar_acc_empty(a), 128);
@@ -164,10 +170,11 @@ __global__ void __launch_bounds__(192, 1)
         }
         if (new_group) {
           gi = p.plan.g_info[g];
-          if (b_loads > 0 && !mbar_wait(bar_b_empty, (b_loads - 1) & 1, abort_flag, p.err)) break;
-          mbar_arrive_expect_tx(bar_b_full, C::B_BYTES);
+          const int u = b_loads % C::BSLOTS, use = b_loads / C::BSLOTS;
+          if (use > 0 && !mbar_wait(bar_b_empty(u), (use - 1) & 1, abort_flag, p.err)) break;
+          mbar_arrive_expect_tx(bar_b_full(u), C::B_BYTES);
           for (int kb = 0; kb < KB; ++kb)
-            tma_load_3d(sbase + C::OFF_B + kb * C::N * 128, &tm_q, bar_b_full, kb * 64, 0, gi.y);
+            tma_load_3d(sbase + C::OFF_B + u * C::B_BYTES + kb * C::N * 128, &tm_q, bar_b_full(u), kb * 64, 0, gi.y);
           ++b_loads;
           b_pending = true;
         }
@@ -206,7 +213,9 @@ __global__ void __launch_bounds__(192, 1)
       if (*abort_flag) {  // let every issued copy land before the block goes away
         for (int s = 0; s < C::STAGES; ++s)
           if (pend[s] >= 0) mbar_wait_drain(bar_a_full(s), (uint32_t)pend[s]);
-        if (b_pending) mbar_wait_drain(bar_b_full, (uint32_t)((b_loads - 1) & 1));
+        if (b_pending)
+          for (int v = b_loads > C::BSLOTS ? b_loads - C::BSLOTS : 0; v < b_loads; ++v)
+            mbar_wait_drain(bar_b_full(v % C::BSLOTS), (uint32_t)((v / C::BSLOTS) & 1));
       }
     }
   } else if (warp == 1) {
@@ -228,14 +237,14 @@ __global__ void __launch_bounds__(192, 1)
           new_group = true;
         }
         if (new_group) {
-          if (!mbar_wait(bar_b_full, b_uses & 1, abort_flag, p.err)) break;
+          if (!mbar_wait(bar_b_full(b_uses % C::BSLOTS), (b_uses / C::BSLOTS) & 1, abort_flag, p.err)) break;
           ++b_uses;
         }
         if (!mbar_wait(bar_a_full(stage), phase, abort_flag, p.err)) break;
         if (!mbar_wait(bar_acc_empty(acc), acc_phase ^ 1, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t a_base = sbase + C::OFF_A + stage * C::A_BYTES;
-        const uint32_t b_base = sbase + C::OFF_B;
+        const uint32_t b_base = sbase + C::OFF_B + ((b_uses - 1) % C::BSLOTS) * C::B_BYTES;
         const uint32_t d = tmem + acc * C::N;
 #pragma unroll
         for (int kb = 0; kb < KB; ++kb) {
@@ -248,7 +257,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         mma_commit(bar_a_empty(stage));
         mma_commit(bar_acc_full(acc));
-        if (item + 1 >= g_next || item + 1 == w1) mma_commit(bar_b_empty);
+        if (item + 1 >= g_next || item + 1 == w1) mma_commit(bar_b_empty((b_uses - 1) % C::BSLOTS));
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
@@ -297,15 +306,13 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
       for (int q = 0; q < G; ++q) {
         float score = 0.f;
+        uint32_t r[NH];  // all head columns of this query, one wait
 #pragma unroll
-        for (int hc = 0; hc < NH / 16; ++hc) {
-          uint32_t r[16];
-          tmem_ld16(tbase + q * NH + hc * 16, r);
-          tmem_wait_ld();
+        for (int hc = 0; hc < NH / 16; ++hc)
+          tmem_ld16(tbase + q * NH + hc * 16, *reinterpret_cast<uint32_t(*)[16]>(r + hc * 16));
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            score = fmaf(w_s[q * NH + hc * 16 + j], fmaxf(__uint_as_float(r[j]), 0.f), score);
-        }
+        for (int j = 0; j < NH; ++j) score = fmaf(w_s[q * NH + j], fmaxf(__uint_as_float(r[j]), 0.f), score);
         if (!bad && q < gi.z && s < qn[q]) p.scores[(int64_t)(gi.y + q) * p.ld + s] = score;
       }
       tc_fence_before();

@@ -27,8 +27,10 @@
 // mbarrier per block.  (The 80-dim test latent uses 16-byte cp.async copies.)
 //
 // Split over a cluster: the selected rows of one query are divided among the
-// blocks of a thread-block cluster; each block keeps its partial (m, l, O) and
-// the cluster combines them through distributed shared memory, so partial
+// blocks of a thread-block cluster; each block keeps its partial (m, l, O).
+// The cluster combines them through distributed shared memory: each block
+// pushes (remote stores, no round trips) its (m, l) to every block and its
+// scaled partial output to the block owning each value slice, so partial
 // outputs never travel through global memory.
 //
 // Warp roles (416 threads, one block per SM):
@@ -47,6 +49,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // raise the running max only past 2^8
 constexpr int kSoftmaxThreads = 256;
+constexpr int kMaxSplit = 8;  // blocks per cluster (splits of one query's rows)
 
 template <int NB, int MB, bool PSEP, bool TMA4>
 struct MlaCfg {
@@ -63,8 +66,9 @@ struct MlaCfg {
   static constexpr int OFF_ALPHA = OFF_MRUN + 64 * 4;                        // 64 float
   static constexpr int OFF_ML = OFF_ALPHA + 64 * 4;                          // 2 x 64 float (m, l)
   static constexpr int OFF_F = OFF_ML + 2 * 64 * 4;                          // 64 float
-  static constexpr int OFF_BAR = OFF_F + 64 * 4;
-  static constexpr int N_BARS = 2 * NB + 7;
+  static constexpr int OFF_MLT = OFF_F + 64 * 4;                             // [kMaxSplit][2][64] pushed (m, l)
+  static constexpr int OFF_BAR = OFF_MLT + kMaxSplit * 2 * 64 * 4;
+  static constexpr int N_BARS = 2 * NB + 8;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr int TMEM_COLS = (MB * 64 + 64) <= 128 ? 128 : (MB * 64 + 64) <= 256 ? 256 : 512;
@@ -145,7 +149,9 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
   float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
   float* ml_s = reinterpret_cast<float*>(smem + C::OFF_ML);
   float* f_s = reinterpret_cast<float*>(smem + C::OFF_F);
-  float* obuf = reinterpret_cast<float*>(smem + C::OFF_KV);  // [64][d_v] after the last tile
+  float* mlt_s = reinterpret_cast<float*>(smem + C::OFF_MLT);  // [split][m or l][head]
+  // combine buffers after the last tile (bf16 receive and staging areas)
+  __nv_bfloat16* obuf_h = reinterpret_cast<__nv_bfloat16*>(smem + C::OFF_KV);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -158,6 +164,7 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
   const uint32_t bar_o_done = smem_u32(bars + 2 * NB + 3);
   const uint32_t bar_drain = smem_u32(bars + 2 * NB + 4);
   auto bar_valid = [&](int par) { return smem_u32(bars + 2 * NB + 5 + par); };
+  const uint32_t bar_recv = smem_u32(bars + 2 * NB + 7);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
@@ -180,6 +187,7 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
     mbar_init(bar_drain, 1);
     mbar_init(bar_valid(0), 128);
     mbar_init(bar_valid(1), 128);
+    mbar_init(bar_recv, 1);
     *abort_flag = 0;
     fence_mbar_init();
     if (TMA4) prefetch_tmap(tm_c);
@@ -370,16 +378,31 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
         alpha_s[st] = alpha;
       }
       rescale = bar_red_or(4, kSoftmaxThreads, rescale);
-      // probabilities, running sums, this key's P^T row for heads h0..h0+31 (bf16)
+      // probabilities, running sums, this key's P^T row for heads h0..h0+31 (bf16).
+      // Without a rescale every alpha is 1 (or the sum is still 0), so the
+      // running sums only add.
+      if (rescale) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 a4 = *reinterpret_cast<const float4*>(alpha_s + h0 + i);
+          lsum[i] *= a4.x; lsum[i + 1] *= a4.y; lsum[i + 2] *= a4.z; lsum[i + 3] *= a4.w;
+        }
+      }
       const uint32_t prow = sbase + C::OFF_P + row * 128;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        float pv[8];
+        float pv[8], mref[8];
+        {
+          const float4 ma = *reinterpret_cast<const float4*>(mrun_s + h0 + cc * 8);
+          const float4 mb4 = *reinterpret_cast<const float4*>(mrun_s + h0 + cc * 8 + 4);
+          mref[0] = ma.x; mref[1] = ma.y; mref[2] = ma.z; mref[3] = ma.w;
+          mref[4] = mb4.x; mref[5] = mb4.y; mref[6] = mb4.z; mref[7] = mb4.w;
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int i = cc * 8 + j;
-          pv[j] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - mrun_s[h0 + i]);  // no valid key yet: m is -inf too
-          lsum[i] = fmaf(lsum[i], alpha_s[h0 + i], pv[j]);
+          pv[j] = x[i] == -INFINITY ? 0.f : exp2f(x[i] - mref[j]);  // no valid key yet: m is -inf too
+          lsum[i] += pv[j];
         }
         const int chunk = half * 4 + cc;
         st_shared_v4(prow + ((chunk ^ (row & 7)) << 4), pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]),
@@ -414,18 +437,29 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
   }
 
   // ------------------------------------------------- combine over the cluster
+  // Push model: every block stores its (m, l) per head into every block's
+  // table, then its scaled partial output straight into the shared memory of
+  // the block that owns each value slice; remote stores do not wait for a
+  // round trip, and no block reads another block's memory.
   __syncthreads();
-  cluster_sync();  // (m, l) of every block visible
+  if (threadIdx.x >= 160 && threadIdx.x < 224) {
+    const int h = threadIdx.x - 160;
+    const float m_own = ml_s[h], l_own = ml_s[64 + h];
+    for (uint32_t r = 0; r < csize; ++r) {
+      st_dsmem_f32(dsmem_addr(smem_u32(mlt_s + (crank * 2 + 0) * 64 + h), r), m_own);
+      st_dsmem_f32(dsmem_addr(smem_u32(mlt_s + (crank * 2 + 1) * 64 + h), r), l_own);
+    }
+  }
+  cluster_sync();  // every table complete; every block is past its main loop
   if (threadIdx.x >= 160 && threadIdx.x < 224) {
     const int h = threadIdx.x - 160;
     float M = -INFINITY;
-    for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + h), r)));
+    for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, mlt_s[(r * 2) * 64 + h]);
     float Lsum = 0.f;
     if (M != -INFINITY)
       for (uint32_t r = 0; r < csize; ++r) {
-        const float m_r = ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + h), r));
-        const float l_r = ld_dsmem_f32(dsmem_addr(smem_u32(ml_s + 64 + h), r));
-        if (m_r != -INFINITY) Lsum += l_r * exp2f(m_r - M);
+        const float m_r = mlt_s[(r * 2) * 64 + h];
+        if (m_r != -INFINITY) Lsum += mlt_s[(r * 2 + 1) * 64 + h] * exp2f(m_r - M);
       }
     const float m_own = ml_s[h];
     f_s[h] = (Lsum > 0.f && m_own != -INFINITY) ? exp2f(m_own - M) / Lsum : 0.f;
@@ -433,52 +467,94 @@ __global__ void __launch_bounds__(160 + kSoftmaxThreads, 1)
       L.lse[(int64_t)t * L.H + h] = Lsum > 0.f ? (M + log2f(Lsum)) * kLn2 : -INFINITY;
   }
   __syncthreads();
+  // Scaled partial outputs in bf16, [source block][head][value dim of the
+  // owner's slice]: this block's own slice goes straight into its receive
+  // area, the others into a staging area, one contiguous slice per owner, and
+  // the TMA engine copies each staged slice into its owner's receive area.
+  const int slice = p.d_v / (int)csize;
+  const int rs = slice + 8;  // head row stride (16 bytes of padding spread the banks)
+  const uint32_t slice_bytes = 64u * (uint32_t)rs * 2u;
+  __nv_bfloat16* recv_h = obuf_h;                                 // [csize][64][rs]
+  __nv_bfloat16* send_h = obuf_h + (size_t)csize * 64 * rs;       // [csize][64][rs]
   if (warp >= 5) {
     const int quad = warp & 3;
     const int h0 = ((warp - 5) >> 2) * 32;
-    const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    // The query tile is dead now: each warp transposes 16 heads x 32 value
+    // dims there so that one thread writes 8 consecutive value dims of a head.
+    float* stage = reinterpret_cast<float*>(smem + C::OFF_Q) + (warp - 5) * 512;
     for (int mb = 0; mb < MB; ++mb) {
-      const int v = mb * 128 + row;
       uint32_t r[32];
       if (my_tiles > 0) {
         tmem_ld32(lane_base + mb * 64 + h0, r);
         tmem_wait_ld();
       }
-      if (v < p.d_v) {
+      const int vq = mb * 128 + quad * 32;  // this warp's first value dim (warp-uniform)
+      if (vq < p.d_v) {
+        const int owner = vq / slice;
+        const int vvq = vq - owner * slice;
+        __nv_bfloat16* dst = owner == (int)crank ? recv_h + (size_t)crank * 64 * rs
+                                                 : send_h + (size_t)owner * 64 * rs;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int h = h0 + j;
-          obuf[h * p.d_v + v] = my_tiles > 0 ? __uint_as_float(r[j]) * f_s[h] : 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int h = h0 + hh * 16 + j;
+            stage[j * 32 + lane] = my_tiles > 0 ? __uint_as_float(r[hh * 16 + j]) * f_s[h] : 0.f;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {  // a warp reads 4 heads' 32 value dims (512 contiguous bytes)
+            const int hl = k * 4 + (lane >> 3), c4 = lane & 7;
+            const float4 a4 = *reinterpret_cast<const float4*>(stage + hl * 32 + 4 * c4);
+            const int h = h0 + hh * 16 + hl;
+            st_shared_v2(smem_u32(dst + h * rs + vvq + 4 * c4), pack_bf16x2(a4.x, a4.y), pack_bf16x2(a4.z, a4.w));
+          }
+          __syncwarp();
         }
       }
     }
+    fence_proxy_async_smem();  // staged slices are read by the TMA engine next
   }
   __syncthreads();
-  cluster_sync();  // every block's scaled partial output is in its shared memory
+  if (threadIdx.x == 160 && csize > 1) {
+    mbar_arrive_expect_tx(bar_recv, (csize - 1) * slice_bytes);
+    for (uint32_t o = 0; o < csize; ++o) {
+      if (o == crank) continue;
+      bulk_copy_smem_to_peer(dsmem_addr(smem_u32(recv_h + (size_t)crank * 64 * rs), o),
+                             smem_u32(send_h + (size_t)o * 64 * rs), slice_bytes, dsmem_addr(bar_recv, o));
+    }
+  }
+  if (csize > 1) {
+    bool ok = true;
+    if (warp >= 5) ok = mbar_wait(bar_recv, 0, abort_flag, p.err);  // every peer's slice has landed
+    (void)ok;
+    __syncthreads();
+  }
   {
-    const int slice = p.d_v / (int)csize;    // value dims this block writes
     const int v0 = (int)crank * slice;
     const int per_h = slice / 4;
     const int items = L.H * per_h;
     for (int it = threadIdx.x; it < items; it += C::THREADS) {
       const int h = it / per_h;
-      const int v = v0 + (it % per_h) * 4;
-      const uint32_t local = smem_u32(obuf + h * p.d_v + v);
+      const int vv = (it % per_h) * 4;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (uint32_t r = 0; r < csize; ++r) {
-        const float4 o = ld_dsmem_f32x4(dsmem_addr(local, r));
-        acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
+        const uint2 o = *reinterpret_cast<const uint2*>(recv_h + ((int)r * 64 + h) * rs + vv);
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+        acc.x += lo.x; acc.y += lo.y; acc.z += hi.x; acc.w += hi.y;
       }
       uint2 packed;
       packed.x = pack_bf16x2(acc.x, acc.y);
       packed.y = pack_bf16x2(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(L.out + ((int64_t)t * L.H + h) * p.d_v + v) = packed;
+      *reinterpret_cast<uint2*>(L.out + ((int64_t)t * L.H + h) * p.d_v + v0 + vv) = packed;
     }
   }
+  // no block may leave while a peer's copy could still read its staging area
+  if (csize > 1) cluster_sync();
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // peers are done reading this block's shared memory
   if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
@@ -539,8 +615,10 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   const int units = a.T * a.n_layers;
   const int tiles_max = (std::min(a.k, a.max_n) + 127) / 128;
   int c = 1;
-  while (c * 2 <= g_max_cluster_mla[which] && c * 2 <= tiles_max && (int64_t)units * c * 2 <= a.num_sms) c *= 2;
-  while (c > 1 && a.d_v % (4 * c) != 0) c /= 2;
+  while (c * 2 <= std::min(g_max_cluster_mla[which], kMaxSplit) && c * 2 <= tiles_max && (int64_t)units * c * 2 <= a.num_sms)
+    c *= 2;
+  // every block owns a value slice of >= 32 dims (one warp's rows push to one owner)
+  while (c > 1 && (a.d_v % (32 * c) != 0)) c /= 2;
 
   MlaParams p;
   for (int l = 0; l < DSA_MAX_LAYERS; ++l) p.layer[l] = a.layer[l < a.n_layers ? l : 0];

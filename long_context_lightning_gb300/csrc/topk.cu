@@ -7,8 +7,7 @@
 // c of the cluster owns a contiguous chunk of the row.  Scores become
 // order-preserving 32-bit keys (-0.0 folded onto +0.0) and a three-digit radix
 // select (11 + 11 + 10 bits) finds the k-th largest key: each digit is a
-// shared-memory histogram per block (lanes of a warp that hit the same bin are
-// merged with match.any before one atomic), summed across the cluster through
+// shared-memory histogram per block, summed across the cluster through
 // distributed shared memory.  Each block then knows how many of its keys are
 // above the threshold and how many equal it; equal keys are granted to the
 // lowest positions first.  The ordered write is per warp: each warp owns a
@@ -43,33 +42,6 @@ struct TopkParams {
   int* err;
 };
 
-// Exclusive scan of one int per thread over the block; *total gets the sum.
-__device__ __forceinline__ int block_scan(int v, int* wsum, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int s = wsum[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, s, o);
-      if (lane >= o) s += y;
-    }
-    wsum[lane] = s;
-  }
-  __syncthreads();
-  const int r = (warp ? wsum[warp - 1] : 0) + x - v;
-  *total = wsum[kWarps - 1];
-  __syncthreads();
-  return r;
-}
-
 __device__ __forceinline__ int warp_excl_scan(int v) {
   const int lane = threadIdx.x & 31;
   int x = v;
@@ -87,10 +59,8 @@ __device__ __forceinline__ int warp_sum(int v) {
   return v;
 }
 
-// Every lane of the warp calls this with the same control flow.
 __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active) {
-  const unsigned m = __match_any_sync(0xffffffffu, active ? bin : 0xffffffffu);
-  if (active && (threadIdx.x & 31) == (unsigned)(__ffs(m) - 1)) atomicAdd(&h[bin], (uint32_t)__popc(m));
+  if (active) atomicAdd(&h[bin], 1u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
@@ -98,7 +68,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   uint32_t* hist = sm;                    // [3][kBins] this block's digit histograms
   uint32_t* tot = sm + 3 * kBins;         // [kBins] cluster-summed histogram of the current digit
   uint32_t* cache = sm + 4 * kBins;       // [cache_keys]
-  __shared__ int wsum[32];
   __shared__ int w_gt[kWarps], w_eq[kWarps], w_eqb[kWarps], w_selb[kWarps];
   __shared__ uint32_t s_digit, s_rem, s_local_above;
   __shared__ uint32_t s_xch[2];           // this block's (keys above threshold, keys equal to it)
@@ -141,22 +110,31 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     uint32_t* h = hist + pass * kBins;
     // ---- histogram of this digit over keys matching the prefix
     if (pass == 0) {
-      for (int i0 = 0; i0 < len; i0 += kThreads * 4) {
-        const int i = i0 + threadIdx.x * 4;
-        const int s = c0 + i;
-        float v[4] = {0.f, 0.f, 0.f, 0.f};
-        if (s + 3 < c1) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(row + s));
-          v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
-        } else {
-          for (int j = 0; j < 4; ++j) if (s + j < c1) v[j] = row[s + j];
+      // four 16-byte loads in flight per thread before any is used
+      for (int i0 = 0; i0 < len; i0 += kThreads * 16) {
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + (u * kThreads + (int)threadIdx.x) * 4;
+          const int s = c0 + i;
+          if (s + 3 < c1) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(row + s));
+            v[4 * u] = f.x; v[4 * u + 1] = f.y; v[4 * u + 2] = f.z; v[4 * u + 3] = f.w;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) v[4 * u + j] = (s + j < c1) ? row[s + j] : 0.f;
+          }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool in = s + j < c1;
-          const uint32_t key = ordered_key(v[j]);
-          if (cached && in) cache[i + j] = key;
-          hist_add(h, key >> sh, in);
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + (u * kThreads + (int)threadIdx.x) * 4;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const bool in = c0 + i + j < c1;
+            const uint32_t key = ordered_key(v[4 * u + j]);
+            if (cached && in) cache[i + j] = key;
+            hist_add(h, key >> sh, in);
+          }
         }
       }
     } else {
@@ -168,47 +146,59 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
       }
     }
     cluster_sync();  // every block's histogram of this digit is complete
-    // ---- cluster-wide histogram
+    // ---- cluster-wide histogram and the digit holding the rem-th largest key.
+    // Thread t owns the bins just below those of thread t-1 (thread 0 the top
+    // ones); it sums them over the cluster, and one block scan of (cluster
+    // count, own count) pairs gives, at the chosen digit, both the keys above
+    // it in the cluster and this block's own keys above it.
     const int nb = (int)msk + 1;
-    for (int bin = threadIdx.x; bin < nb; bin += kThreads) {
+    const int bpt = nb / kThreads;  // 2 or 1 bins per thread
+    const int top = nb - 1 - (int)threadIdx.x * bpt;
+    int tot_mine = 0, own_mine = 0;
+    for (int j = 0; j < bpt; ++j) {
+      const int bin = top - j;
       uint32_t sum = h[bin];
       const uint32_t local = smem_u32(h + bin);
       for (uint32_t r = 0; r < csize; ++r)
         if (r != crank) sum += ld_dsmem_u32(dsmem_addr(local, r));
       tot[bin] = sum;
+      tot_mine += (int)sum;
+      own_mine += (int)h[bin];
+    }
+    const int tot_ex = warp_excl_scan(tot_mine), own_ex = warp_excl_scan(own_mine);
+    if (lane == 31) {
+      w_gt[warp] = tot_ex + tot_mine;  // warp totals (reusing the write-phase scratch)
+      w_eq[warp] = own_ex + own_mine;
     }
     __syncthreads();
-    // ---- the digit holding the rem-th largest key: suffix sums from the top bin
-    {
-      const int per_t = (nb + kThreads - 1) / kThreads;  // 2 or 1
-      const int hi = nb - 1 - threadIdx.x * per_t;       // this thread's bins: hi, hi-1, ...
-      int mine = 0;
-      for (int j = 0; j < per_t; ++j) if (hi - j >= 0) mine += tot[hi - j];
-      int total;
-      int above = block_scan(mine, wsum, &total);        // keys in bins above this thread's
-      for (int j = 0; j < per_t; ++j) {
-        const int bin = hi - j;
-        if (bin < 0) break;
-        const int cnt = tot[bin];
-        if ((uint32_t)above < rem && rem <= (uint32_t)(above + cnt)) {
-          s_digit = bin;
-          s_rem = rem - above;
-        }
-        above += cnt;
-      }
-      if (threadIdx.x == 0) s_local_above = 0;
-      __syncthreads();
-      const uint32_t d = s_digit;
-      uint32_t la = 0;  // this block's own keys in bins above the chosen digit
-      for (int bin = d + 1 + threadIdx.x; bin < nb; bin += kThreads) la += h[bin];
-      la = warp_sum(la);
-      if (lane == 0 && la) atomicAdd(&s_local_above, la);
-      __syncthreads();
-      local_greater += s_local_above;
-      prefix = (prefix << bits) | d;
-      rem = s_rem;
-      __syncthreads();
+    if (warp == 0) {
+      const int a_t = w_gt[lane], a_o = w_eq[lane];
+      w_eqb[lane] = warp_excl_scan(a_t);
+      w_selb[lane] = warp_excl_scan(a_o);
     }
+    __syncthreads();
+    {
+      int acc_t = w_eqb[warp] + tot_ex, acc_o = w_selb[warp] + own_ex;  // keys above this thread's bins
+      if ((uint32_t)acc_t < rem && rem <= (uint32_t)(acc_t + tot_mine)) {
+        for (int j = 0; j < bpt; ++j) {
+          const int bin = top - j;
+          const int cnt = (int)tot[bin];
+          if ((uint32_t)(acc_t + cnt) >= rem) {
+            s_digit = bin;
+            s_rem = rem - acc_t;
+            s_local_above = acc_o;
+            break;
+          }
+          acc_t += cnt;
+          acc_o += (int)h[bin];
+        }
+      }
+    }
+    __syncthreads();
+    local_greater += s_local_above;
+    prefix = (prefix << bits) | s_digit;
+    rem = s_rem;
+    __syncthreads();  // the next pass rewrites s_digit, s_rem, s_local_above and the scratch
   }
   const uint32_t thr = prefix;  // the k-th largest key
   const uint32_t local_equal = hist[2 * kBins + (thr & 0x3FFu)];
@@ -228,16 +218,28 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   }
   const int take = (int)min(local_equal, rem > eq_before ? rem - eq_before : 0u);
 
-  // ---- ordered write: warp w owns the contiguous range [w0, w1) of the chunk
+  // ---- ordered write: warp w owns the contiguous range [w0, w1) of the chunk.
+  // One counting pass records per lane which of its keys are above / equal to
+  // the threshold as bits (up to 64 keys per lane), so the ordered pass needs
+  // no second read of the keys.
   const int pw = ((len + kWarps - 1) / kWarps + 31) & ~31;
   const int w0 = min(len, warp * pw), w1 = min(len, w0 + pw);
+  const int iters = (w1 - w0 + 31) / 32;
+  const bool in_regs = iters <= 64;
   auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : ordered_key(row[c0 + i]); };
+  uint32_t gt_lo = 0, gt_hi = 0, eq_lo = 0, eq_hi = 0;
   {
     int gt = 0, eq = 0;
-    for (int i = w0 + lane; i < w1; i += 32) {
-      const uint32_t key = key_at(i);
-      gt += key > thr;
-      eq += key == thr;
+    for (int it = 0; it < iters; ++it) {
+      const int i = w0 + it * 32 + lane;
+      const uint32_t key = i < w1 ? key_at(i) : 0u;
+      const uint32_t g = (i < w1 && key > thr), e = (i < w1 && key == thr);
+      gt += g;
+      eq += e;
+      if (in_regs) {
+        if (it < 32) { gt_lo |= g << it; eq_lo |= e << it; }
+        else { gt_hi |= g << (it - 32); eq_hi |= e << (it - 32); }
+      }
     }
     gt = warp_sum(gt);
     eq = warp_sum(eq);
@@ -260,13 +262,21 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     int eq_run = w_eqb[warp];
     int pos_run = (int)base + w_selb[warp];
     const unsigned lt = (1u << lane) - 1u;
-    for (int i0 = w0; i0 < w1; i0 += 32) {
-      const int i = i0 + lane;
-      const bool in = i < w1;
-      const uint32_t key = in ? key_at(i) : 0u;
-      const bool eqf = in && key == thr;
+    for (int it = 0; it < iters; ++it) {
+      const int i = w0 + it * 32 + lane;
+      bool gtf, eqf;
+      if (in_regs) {
+        const uint32_t gw = it < 32 ? gt_lo : gt_hi, ew = it < 32 ? eq_lo : eq_hi;
+        const int sh = it & 31;
+        gtf = (gw >> sh) & 1u;
+        eqf = (ew >> sh) & 1u;
+      } else {
+        const uint32_t key = i < w1 ? key_at(i) : 0u;
+        gtf = i < w1 && key > thr;
+        eqf = i < w1 && key == thr;
+      }
       const unsigned eqm = __ballot_sync(0xffffffffu, eqf);
-      const bool sel = in && (key > thr || (eqf && eq_run + __popc(eqm & lt) < take));
+      const bool sel = gtf || (eqf && eq_run + __popc(eqm & lt) < take);
       const unsigned selm = __ballot_sync(0xffffffffu, sel);
       if (sel) {
         const int pos = pos_run + __popc(selm & lt);
@@ -307,11 +317,11 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
       g_max_cluster = 16;
     cudaGetLastError();
   }
-  // cluster size: one block per row while rows fit its key cache and the rows
-  // alone give a few waves of blocks; more blocks per row for few long rows
+  // cluster size: enough blocks per row that the rows fill a good share of the
+  // GPU (each block reads less of the row), and chunks that fit the key cache
   int c = 1;
   while (c < g_max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
-  while (c < g_max_cluster && (int64_t)a.T * c * 4 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 8192) c *= 2;
+  while (c < g_max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
   const int per = (((a.max_n + c - 1) / c) + 3) & ~3;
   const int cache_keys = per <= kMaxCacheKeys ? per : 0;
   const size_t smem = (size_t)(4 * kBins + cache_keys) * 4;
