@@ -75,7 +75,7 @@ struct MlaCfg {
   static constexpr int OFF_ALPHA = OFF_MREF + 64 * 4;        // 64 float
   static constexpr int OFF_F = OFF_ALPHA + 64 * 4;           // kMaxSplit x 64 float
   static constexpr int OFF_BAR = OFF_F + kMaxSplit * 64 * 4;
-  static constexpr int N_BARS = NB + 9;
+  static constexpr int N_BARS = NB + 10;
   static constexpr int OFF_MISC = OFF_BAR + N_BARS * 8;
   static constexpr int OFF_LAYER = OFF_MISC + 16;          // output, LSE, heads of this block's layer
   static constexpr int SMEM_BYTES = OFF_LAYER + 32 + 1024;
@@ -178,19 +178,21 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
-  // one phase per tile each: the tile landed (bytes of all its blocks); column
-  // block kb read by every MMA of the tile (commit); S^T formed (commit); P^T
-  // written (softmax threads); the tile's valid flags written (gather warp 0)
-  const uint32_t bar_full = smem_u32(bars);
-  auto bar_empty = [&](int kb) { return smem_u32(bars + 1 + kb); };
-  const uint32_t bar_s_full = smem_u32(bars + NB + 1);
-  const uint32_t bar_p_full = smem_u32(bars + NB + 2);
-  const uint32_t bar_valid = smem_u32(bars + NB + 3);
-  const uint32_t bar_q_full = smem_u32(bars + NB + 4);
-  const uint32_t bar_o_done = smem_u32(bars + NB + 5);
-  const uint32_t bar_drain = smem_u32(bars + NB + 6);
-  const uint32_t bar_recv = smem_u32(bars + NB + 7);   // peers' slabs landed (bytes)
-  const uint32_t bar_ready = smem_u32(bars + NB + 8);  // peers' tile memory free (remote arrivals)
+  // one phase per tile each: column blocks [0, NB_A) / [NB_A, NB) of the tile
+  // landed (bytes); column block kb read by every MMA of the tile (commit);
+  // S^T formed (commit); P^T written (softmax threads); the tile's valid flags
+  // written (gather warp 0)
+  constexpr int NB_A = (NB + 1) / 2;  // blocks of the first S^T run
+  auto bar_full = [&](int part) { return smem_u32(bars + part); };
+  auto bar_empty = [&](int kb) { return smem_u32(bars + 2 + kb); };
+  const uint32_t bar_s_full = smem_u32(bars + NB + 2);
+  const uint32_t bar_p_full = smem_u32(bars + NB + 3);
+  const uint32_t bar_valid = smem_u32(bars + NB + 4);
+  const uint32_t bar_q_full = smem_u32(bars + NB + 5);
+  const uint32_t bar_o_done = smem_u32(bars + NB + 6);
+  const uint32_t bar_drain = smem_u32(bars + NB + 7);
+  const uint32_t bar_recv = smem_u32(bars + NB + 8);   // peers' slabs landed (bytes)
+  const uint32_t bar_ready = smem_u32(bars + NB + 9);  // peers' tile memory free (remote arrivals)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();
@@ -204,7 +206,8 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   const uint32_t slab_bytes = (uint32_t)(kSlabHeader + slice * kSlabRowWords * 4);
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_full, 1);
+    mbar_init(bar_full(0), 1);
+    mbar_init(bar_full(1), 1);
     for (int kb = 0; kb < NB; ++kb) mbar_init(bar_empty(kb), 1);
     mbar_init(bar_valid, 32);
     mbar_init(bar_s_full, 1);
@@ -293,12 +296,14 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) valid_s[4 * lane + k] = v4[k];
             mbar_arrive(bar_valid);
-            // one arrival with the whole tile's bytes opens the tile's phase;
-            // blocks of other warps may land before it (the count goes negative)
-            if (lane == 0) mbar_arrive_expect_tx(bar_full, C::STAGE);
+            // one arrival with the first part's bytes opens its phase; blocks of
+            // other warps may land before it (the count goes negative)
+            if (lane == 0) mbar_arrive_expect_tx(bar_full(0), NB_A * kBlk);
           }
+          if (kb == NB - 1 && lane == 0) mbar_arrive_expect_tx(bar_full(1), (NB - NB_A) * kBlk);
           __syncwarp();
-          if (!bad) tma_gather4(dst + kb * kBlk, tm_c, bar_full, kb * 64, r4[0], r4[1], r4[2], r4[3]);
+          const uint32_t bar = bar_full(kb < NB_A ? 0 : 1);
+          if (!bad) tma_gather4(dst + kb * kBlk, tm_c, bar, kb * 64, r4[0], r4[1], r4[2], r4[3]);
         }
       }
     } else if (warp == 4) {
@@ -319,14 +324,22 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
         // orders it for the tensor cores.
         for (int jj = 0; jj < my_tiles && !bad; ++jj) {
           const uint32_t par = jj & 1;
-          // S^T = C . Q^T over all D/64 column blocks
-          if (!mbar_wait(bar_full, par, abort_flag, p.err)) { bad = true; break; }
+          // S^T = C . Q^T over all D/64 column blocks, in two runs: the blocks
+          // released first by the previous PV land first
+          if (!mbar_wait(bar_full(0), par, abort_flag, p.err)) { bad = true; break; }
 #pragma unroll
-          for (int kb = 0; kb < NB; ++kb)
+          for (int kb = 0; kb < NB_A; ++kb)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16(tmem + C::S_COL, dk + (uint64_t)((kb * kBlk + kk * 32) >> 4),
                        dq + (uint64_t)((kb * 64 * 128 + kk * 32) >> 4), idesc_s, (kb | kk) != 0);
+          if (!mbar_wait(bar_full(1), par, abort_flag, p.err)) { bad = true; break; }
+#pragma unroll
+          for (int kb = NB_A; kb < NB; ++kb)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tmem + C::S_COL, dk + (uint64_t)((kb * kBlk + kk * 32) >> 4),
+                       dq + (uint64_t)((kb * 64 * 128 + kk * 32) >> 4), idesc_s, 1u);
           mma_commit(bar_s_full);
           // O^T += C^T . P^T over the tile's 128 keys; each column block is
           // released to the gather as soon as the MMAs reading it complete
