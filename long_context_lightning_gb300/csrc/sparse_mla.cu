@@ -528,39 +528,49 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       }
       bool ok = true;
       if (csize > 1) ok = mbar_wait_cluster(bar_recv, 0, p.err);  // every source's slab has landed
-      // weight of each source per head
-      if (st < 64) {
-        float M = -INFINITY;
-        for (uint32_t r = 0; r < csize; ++r) M = fmaxf(M, reinterpret_cast<const float*>(recv + r * slab_bytes)[st]);
-        float Lsum = 0.f;
-        if (M != -INFINITY)
-          for (uint32_t r = 0; r < csize; ++r) {
-            const float* hdr = reinterpret_cast<const float*>(recv + r * slab_bytes);
-            if (hdr[st] != -INFINITY) Lsum += hdr[64 + st] * ex2_approx(hdr[st] - M);
-          }
-        const float inv = rcp_approx(Lsum);
-        for (uint32_t r = 0; r < csize; ++r) {
-          const float m_r = reinterpret_cast<const float*>(recv + r * slab_bytes)[st];
-          f_s[r * 64 + st] = (ok && Lsum > 0.f && m_r != -INFINITY) ? ex2_approx(m_r - M) * inv : 0.f;
-        }
-        if (crank == 0 && lo.lse != nullptr && st < lo.H)
-          lo.lse[(int64_t)t * lo.H + st] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
+      // weight of each source per head: four threads per head, each with the
+      // sources sub and sub + 4; max and sum over a head's sources by shuffles
+      {
+        const int h = st >> 2, sub = st & 3;
+        const float* h0p = reinterpret_cast<const float*>(recv + sub * slab_bytes);
+        const float* h1p = reinterpret_cast<const float*>(recv + (sub + 4) * slab_bytes);
+        const bool has0 = sub < (int)csize, has1 = sub + 4 < (int)csize;
+        const float m0 = has0 ? h0p[h] : -INFINITY, m1 = has1 ? h1p[h] : -INFINITY;
+        const float l0 = has0 ? h0p[64 + h] : 0.f, l1 = has1 ? h1p[64 + h] : 0.f;
+        float M = fmaxf(m0, m1);
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+        const float e0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M), e1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+        float Lsum = l0 * e0 + l1 * e1;
+        Lsum += __shfl_xor_sync(0xffffffffu, Lsum, 1);
+        Lsum += __shfl_xor_sync(0xffffffffu, Lsum, 2);
+        const float inv = (ok && Lsum > 0.f) ? rcp_approx(Lsum) : 0.f;
+        if (has0) f_s[sub * 64 + h] = e0 * inv;
+        if (has1) f_s[(sub + 4) * 64 + h] = e1 * inv;
+        if (sub == 0 && crank == 0 && lo.lse != nullptr && h < lo.H)
+          lo.lse[(int64_t)t * lo.H + h] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
       }
       named_bar_sync(3, kSoftmaxThreads);
       // this block's value slice of every head: lanes walk the value dims
+      // (slice is a power of two: d_v and the cluster size are)
       const int v0 = (int)crank * slice;
+      const int ls = __ffs(slice) - 1;
       const int items = 32 * slice;  // (head pair, value dim)
       for (int it = st; it < items; it += kSoftmaxThreads) {
-        const int hp = it / slice;
-        const int v = it - hp * slice;
+        const int hp = it >> ls;
+        const int v = it & (slice - 1);
         const int h = 2 * hp;
         if (h >= lo.H) continue;
         float a0 = 0.f, a1 = 0.f;
-        for (uint32_t r = 0; r < csize; ++r) {
-          const uint32_t w =
-              reinterpret_cast<const uint32_t*>(recv + r * slab_bytes + kSlabHeader)[v * kSlabRowWords + hp];
-          a0 = fmaf(f_s[r * 64 + h], bf16lo_to_f32(w), a0);
-          a1 = fmaf(f_s[r * 64 + h + 1], bf16hi_to_f32(w), a1);
+#pragma unroll
+        for (int r = 0; r < kMaxSplit; ++r) {
+          if (r < (int)csize) {
+            const uint32_t w =
+                reinterpret_cast<const uint32_t*>(recv + r * slab_bytes + kSlabHeader)[v * kSlabRowWords + hp];
+            const float2 f2 = reinterpret_cast<const float2*>(f_s + r * 64)[hp];
+            a0 = fmaf(f2.x, bf16lo_to_f32(w), a0);
+            a1 = fmaf(f2.y, bf16hi_to_f32(w), a1);
+          }
         }
         lo.out[((int64_t)t * lo.H + h) * lo.d_v + v0 + v] = __float2bfloat16_rn(a0);
         if (h + 1 < lo.H) lo.out[((int64_t)t * lo.H + h + 1) * lo.d_v + v0 + v] = __float2bfloat16_rn(a1);
