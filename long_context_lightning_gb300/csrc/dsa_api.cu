@@ -149,7 +149,8 @@ dsa_status_t launch_indexer_call(const dsa_batch_t* b, const dsa_indexer_t* ix, 
 }
 
 dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t ld, int32_t k, int32_t* idx,
-                              int64_t ld_idx, const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream) {
+                              int64_t ld_idx, const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream,
+                              bool plan_early = false) {
   TopkLaunch a;
   a.scores = scores;
   a.ld_scores = ld;
@@ -161,12 +162,14 @@ dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t
   a.q_n = plan.q_n;
   a.err = dev.err;
   a.num_sms = dev.num_sms;
+  a.plan_early = plan_early;
   return launch_topk(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_layer_t* layers,
                              void* const* outs, float* const* lses, const int32_t* idx, int64_t ld_idx, int32_t k,
-                             const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream) {
+                             const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream,
+                             bool plan_early = false) {
   MlaLaunch a;
   std::memset(&a, 0, sizeof(a));
   for (int l = 0; l < n_layers; ++l) {
@@ -189,6 +192,7 @@ dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_l
   a.q_n = plan.q_n;
   a.err = dev.err;
   a.num_sms = dev.num_sms;
+  a.plan_early = plan_early;
   return launch_sparse_mla(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -429,9 +433,11 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
   const int64_t ld = (int64_t)scores_ld(batch);
   if ((s = launch_indexer_call(batch, indexer, scores, ld, plan, dev, stream)) != DSA_OK) return s;
   if (!mark(2)) return DSA_ERR_CUDA;
-  if ((s = launch_topk_call(batch, scores, ld, topk, idx, ld_idx, plan, dev, stream)) != DSA_OK) return s;
+  // the plan kernel ran two launches before the top-k and three before the MLA
+  if ((s = launch_topk_call(batch, scores, ld, topk, idx, ld_idx, plan, dev, stream, true)) != DSA_OK) return s;
   if (!mark(3)) return DSA_ERR_CUDA;
-  if ((s = launch_mla_call(batch, n_layers, layers, outs, lses, idx, ld_idx, topk, plan, dev, stream)) != DSA_OK)
+  if ((s = launch_mla_call(batch, n_layers, layers, outs, lses, idx, ld_idx, topk, plan, dev, stream, true)) !=
+      DSA_OK)
     return s;
   return mark(4) ? DSA_OK : DSA_ERR_CUDA;
 }

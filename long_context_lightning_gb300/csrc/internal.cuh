@@ -122,6 +122,9 @@ struct TopkLaunch {
   const int32_t* q_n;
   int* err;
   int num_sms;
+  // the plan kernel is not the immediately preceding launch: its outputs are
+  // complete before this grid starts and may be read before griddepcontrol.wait
+  bool plan_early = false;
 };
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream);
 
@@ -147,6 +150,7 @@ struct MlaLaunch {
   const int32_t* q_n;
   int* err;
   int num_sms;
+  bool plan_early = false;  // as in TopkLaunch
 };
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
 

@@ -102,6 +102,7 @@ struct MlaParams {
   const int32_t* q_seq;
   const int32_t* q_n;
   int* err;
+  int32_t plan_early;
 };
 
 __device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
@@ -249,11 +250,21 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   int my_tiles = 0;
   // ------------------------------------------------ the tiles of this block
   auto run_tiles = [&]() {
+    // The plan is read before the wait when it was written two or more grids
+    // back (complete before this grid could start); L2 loads, no stale L1.
+    // The sequence's first pool row of a contiguous cache is a caller input.
+    int n_t = 0, b = 0;
+    int64_t seq_base = 0;
+    auto read_plan = [&]() {
+      n_t = __ldcg(p.q_n + t);
+      b = __ldcg(p.q_seq + t);
+      if (!L.kv.paged && b >= 0) seq_base = __ldg(L.kv.seq_start + b);
+    };
+    if (p.plan_early) read_plan();
     pdl_wait();  // positions and plan of the previous grids are complete from here on
     pdl_trigger();
+    if (!p.plan_early) read_plan();
 
-    const int n_t = p.q_n[t];
-    const int b = p.q_seq[t];
     const int nvalid = min(n_t, p.k);
     const int tiles = (nvalid + kRows - 1) / kRows;
     const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
@@ -281,7 +292,12 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
           }
           int64_t row = -1;
           if (pos >= 0) {
-            row = cache_row(L.kv, b, pos);
+            if (L.kv.paged) {
+              row = cache_row(L.kv, b, pos);
+            } else {
+              row = seq_base + pos;
+              if (row < 0 || row >= L.kv.num_rows) row = -1;
+            }
             if (row < 0 && warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
           }
           v4[k] = row >= 0;
@@ -659,6 +675,7 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   p.q_seq = a.q_seq;
   p.q_n = a.q_n;
   p.err = a.err;
+  p.plan_early = a.plan_early ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c, units, 1);

@@ -40,6 +40,7 @@ struct TopkParams {
   int32_t cache_keys;  // per-block key cache capacity (0: no cache)
   const int32_t* q_n;
   int* err;
+  int32_t plan_early;  // the plan was written two or more grids back
 };
 
 __device__ __forceinline__ int warp_excl_scan(int v) {
@@ -75,9 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   const int t = blockIdx.y;
   const uint32_t crank = cluster_ctarank();
   const uint32_t csize = cluster_nctarank();
+  int n = p.plan_early ? __ldcg(p.q_n + t) : 0;
   pdl_wait();  // scores and plan of the previous grids are complete from here on
   pdl_trigger();
-  const int n = p.q_n[t];
+  if (!p.plan_early) n = p.q_n[t];
   const int k = p.k;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int32_t* out = p.idx + (int64_t)t * p.ld_idx;
@@ -338,6 +340,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   p.cache_keys = cache_keys;
   p.q_n = a.q_n;
   p.err = a.err;
+  p.plan_early = a.plan_early ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c, a.T, 1);
