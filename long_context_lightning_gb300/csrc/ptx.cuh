@@ -156,6 +156,12 @@ __device__ __forceinline__ void bulk_copy_smem_to_peer(uint32_t dst_cluster, uin
                "r"(src_cta), "r"(bytes), "r"(bar_cluster)
                : "memory");
 }
+// Asynchronous prefetch of the global bytes [addr, addr + bytes) into L2; no
+// completion is signalled.  addr 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(addr)), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -278,10 +278,9 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       // completed; S^T waits for the whole tile.
       const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
       bool bad = false;
-      for (int jj = 0; jj < my_tiles; ++jj) {
-        const uint32_t par = (jj & 1) ^ 1;  // phase of the previous tile
-        int32_t r4[4];
-        bool v4[4];
+      int32_t r4[4];
+      bool v4[4];
+      auto resolve = [&](int jj) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int e = (j0 + jj) * kRows + 4 * lane + k;
@@ -303,6 +302,10 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
           v4[k] = row >= 0;
           r4[k] = row >= 0 ? (int32_t)row : 0;  // an unused slot reads pool row 0 (finite data; weight 0)
         }
+      };
+      if (my_tiles > 0) resolve(0);
+      for (int jj = 0; jj < my_tiles; ++jj) {
+        const uint32_t par = (jj & 1) ^ 1;  // phase of the previous tile
         const uint32_t dst = sbase + C::OFF_KV + lane * 512;
         for (int kb = warp; kb < NB; kb += 4) {
           bad |= !mbar_wait(bar_empty(kb), par, abort_flag, p.err);
@@ -320,6 +323,20 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
           __syncwarp();
           const uint32_t bar = bar_full(kb < NB_A ? 0 : 1);
           if (!bad) tma_gather4(dst + kb * kBlk, tm_c, bar, kb * 64, r4[0], r4[1], r4[2], r4[3]);
+        }
+        if (jj + 1 < my_tiles) {
+          // Shared memory holds one tile.  Once this tile has landed, HBM is idle
+          // while it is consumed: the next tile's rows stream into L2 then, and
+          // its gathers read L2.  The four warps split the rows (lane l, warp w:
+          // row 4l + w), one bulk prefetch of a whole row each.
+          resolve(jj + 1);
+          int32_t rp = r4[0];
+          bool vp = v4[0];
+#pragma unroll
+          for (int k = 1; k < 4; ++k)
+            if (warp == k) { rp = r4[k]; vp = v4[k]; }
+          if (!bad) bad = !mbar_wait(bar_full(1), jj & 1, abort_flag, p.err);
+          if (!bad && vp) prefetch_l2_bulk(L.kv.base + (int64_t)rp * L.kv.row_stride, (uint32_t)p.d_qk * 2u);
         }
       }
     } else if (warp == 4) {
@@ -511,6 +528,9 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
           hdr[64 + st] = l_own;
         }
       }
+      // one-shot code: kept a loop, since every unrolled copy would be a fresh
+      // instruction fetch
+#pragma unroll 1
       for (int mb = 0; mb < MB; ++mb) {
         const int vq = mb * 128 + quad * 32;  // this warp's first value dim (warp-uniform)
         if (vq >= lo.d_v) continue;
