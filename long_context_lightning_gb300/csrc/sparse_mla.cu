@@ -61,7 +61,6 @@ constexpr int kMaxSplit = 8;          // blocks per cluster (splits of one query
 constexpr int kRows = 128;            // selected rows per tile
 constexpr int kBlk = kRows * 128;     // one [128 rows x 64 dims] bf16 block
 constexpr int kSlabHeader = 512;      // (m, l) x 64 heads, fp32
-constexpr int kSlabRowWords = 33;     // 64 bf16 heads + one pad word per value dim
 
 template <int NB, int MB>
 struct MlaCfg {
@@ -204,7 +203,9 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   const CUtensorMap* tm_q = li == 0 ? &tm_q0 : li == 1 ? &tm_q1 : li == 2 ? &tm_q2 : &tm_q3;
   const CUtensorMap* tm_c = li == 0 ? &tm_c0 : li == 1 ? &tm_c1 : li == 2 ? &tm_c2 : &tm_c3;
   const int slice = p.d_v / (int)csize;  // value dims owned by each block of the cluster
-  const uint32_t slab_bytes = (uint32_t)(kSlabHeader + slice * kSlabRowWords * 4);
+  // a slab: header, then [32 head pairs][slice value dims] words (bf16 pairs)
+  const uint32_t slab_bytes = (uint32_t)(kSlabHeader + slice * 32 * 4);
+  const int ls = __ffs(slice) - 1;  // slice is a power of two (d_v and the cluster size are)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_full(0), 1);
@@ -505,8 +506,8 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     // ------------------------------------------------- combine over the cluster
     // Every role is past its loop: this block's stages are free for the slabs.
     // recv: [source block][slab], send: [owner block][slab]; a slab is the
-    // source's (m, l) per head, then [value dim of the owner's slice] rows of 64
-    // bf16 heads and one pad word.
+    // source's (m, l) per head, then one row per head pair of the owner's
+    // slice of value dims, each word the pair as two bf16.
     __syncthreads();
     const LayerOut lo = *reinterpret_cast<const LayerOut*>(smem + C::OFF_LAYER);
     uint8_t* recv = smem + C::OFF_KV;
@@ -542,13 +543,14 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) r[i] = 0u;
         }
-        const int owner = vq / slice;
-        const int v = vq - owner * slice + lane;
+        const int owner = vq >> ls;  // a slice holds whole warps (>= 32 dims)
+        const int v = vq - (owner << ls) + lane;
         uint8_t* slab = owner == (int)crank ? recv + crank * slab_bytes : send + owner * slab_bytes;
-        uint32_t* rowp = reinterpret_cast<uint32_t*>(slab + kSlabHeader) + v * kSlabRowWords + h0 / 2;
+        // lane = value dim: a warp writes 32 consecutive words of each head-pair row
+        uint32_t* col = reinterpret_cast<uint32_t*>(slab + kSlabHeader) + (h0 / 2) * slice + v;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          rowp[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          col[i * slice] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
       }
       fence_proxy_async_smem();  // the slabs are read by the bulk-copy engine
       named_bar_sync(3, kSoftmaxThreads);
@@ -587,29 +589,37 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
           lo.lse[(int64_t)t * lo.H + h] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
       }
       named_bar_sync(3, kSoftmaxThreads);
-      // this block's value slice of every head: lanes walk the value dims
-      // (slice is a power of two: d_v and the cluster size are)
+      // this block's value slice of every head: a thread takes one head pair and
+      // four consecutive value dims per item (one 16-byte load per source, one
+      // 8-byte store per head); a warp's items are contiguous in every slab
       const int v0 = (int)crank * slice;
-      const int ls = __ffs(slice) - 1;
-      const int items = 32 * slice;  // (head pair, value dim)
+      const int lvg = ls - 2;
+      const int items = 32 << lvg;
+      const float2* fw = reinterpret_cast<const float2*>(f_s);  // [source][head pair]
       for (int it = st; it < items; it += kSoftmaxThreads) {
-        const int hp = it >> ls;
-        const int v = it & (slice - 1);
+        const int hp = it >> lvg;
+        const int vg = it & ((1 << lvg) - 1);
         const int h = 2 * hp;
         if (h >= lo.H) continue;
-        float a0 = 0.f, a1 = 0.f;
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int r = 0; r < kMaxSplit; ++r) {
           if (r < (int)csize) {
-            const uint32_t w =
-                reinterpret_cast<const uint32_t*>(recv + r * slab_bytes + kSlabHeader)[v * kSlabRowWords + hp];
-            const float2 f2 = reinterpret_cast<const float2*>(f_s + r * 64)[hp];
-            a0 = fmaf(f2.x, bf16lo_to_f32(w), a0);
-            a1 = fmaf(f2.y, bf16hi_to_f32(w), a1);
+            const uint4 w = *reinterpret_cast<const uint4*>(recv + r * slab_bytes + kSlabHeader +
+                                                             (size_t)(hp * slice + 4 * vg) * 4);
+            const float2 f2 = fw[r * 32 + hp];
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              a0[j] = fmaf(f2.x, bf16lo_to_f32(ws[j]), a0[j]);
+              a1[j] = fmaf(f2.y, bf16hi_to_f32(ws[j]), a1[j]);
+            }
           }
         }
-        lo.out[((int64_t)t * lo.H + h) * lo.d_v + v0 + v] = __float2bfloat16_rn(a0);
-        if (h + 1 < lo.H) lo.out[((int64_t)t * lo.H + h + 1) * lo.d_v + v0 + v] = __float2bfloat16_rn(a1);
+        __nv_bfloat16* o0 = lo.out + ((int64_t)t * lo.H + h) * lo.d_v + v0 + 4 * vg;
+        *reinterpret_cast<uint2*>(o0) = make_uint2(pack_bf16x2(a0[0], a0[1]), pack_bf16x2(a0[2], a0[3]));
+        if (h + 1 < lo.H)
+          *reinterpret_cast<uint2*>(o0 + lo.d_v) = make_uint2(pack_bf16x2(a1[0], a1[1]), pack_bf16x2(a1[2], a1[3]));
       }
     }
   };
