@@ -271,44 +271,54 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
     my_tiles = j1 - j0;
 
+    // Lane l of a gathering warp resolves rows 4l..4l+3 of a tile to pool rows.
+    const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
+    int32_t r4[4];
+    bool v4[4];
+    auto resolve = [&](int jj) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = (j0 + jj) * kRows + 4 * lane + k;
+        int pos = e < nvalid ? __ldg(idx_row + e) : -1;
+        if (pos >= n_t || pos < -1) {
+          if (warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          pos = -1;
+        }
+        int64_t row = -1;
+        if (pos >= 0) {
+          if (L.kv.paged) {
+            row = cache_row(L.kv, b, pos);
+          } else {
+            row = seq_base + pos;
+            if (row < 0 || row >= L.kv.num_rows) row = -1;
+          }
+          if (row < 0 && warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
+        }
+        v4[k] = row >= 0;
+        r4[k] = row >= 0 ? (int32_t)row : 0;  // an unused slot reads pool row 0 (finite data; weight 0)
+      }
+    };
+    // Column block NB-1 (it holds P^T while the PV runs, so it is released
+    // last) is gathered by the softmax warps, idle at that point: lanes
+    // 4j..4j+3 of softmax warp j, four copies per warp rather than one warp's
+    // thirty-two.
+    auto gather_last_block = [&]() {
+      if ((lane >> 2) == warp - 5)
+        tma_gather4(sbase + C::OFF_KV + lane * 512 + (NB - 1) * kBlk, tm_c, bar_full(1), (NB - 1) * 64, r4[0], r4[1], r4[2],
+                    r4[3]);
+    };
+
     if (warp < 4) {
       // ------------------------------------------------------------ row gather
-      // Warp w owns the column blocks kb = w, w+4, w+8 of every tile; lane l
-      // resolves rows 4l..4l+3 of the tile and gathers them for each of the
-      // warp's blocks.  A block is refilled as soon as the PV that reads it has
-      // completed; S^T waits for the whole tile.
-      const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
+      // Warp w owns the column blocks kb = w, w+4 < NB-1 of every tile and
+      // gathers its lanes' rows for each of them.  A block is refilled as soon
+      // as the PV that reads it has completed; S^T waits for the whole tile.
       bool bad = false;
-      int32_t r4[4];
-      bool v4[4];
-      auto resolve = [&](int jj) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int e = (j0 + jj) * kRows + 4 * lane + k;
-          int pos = e < nvalid ? __ldg(idx_row + e) : -1;
-          if (pos >= n_t || pos < -1) {
-            if (warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
-            pos = -1;
-          }
-          int64_t row = -1;
-          if (pos >= 0) {
-            if (L.kv.paged) {
-              row = cache_row(L.kv, b, pos);
-            } else {
-              row = seq_base + pos;
-              if (row < 0 || row >= L.kv.num_rows) row = -1;
-            }
-            if (row < 0 && warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
-          }
-          v4[k] = row >= 0;
-          r4[k] = row >= 0 ? (int32_t)row : 0;  // an unused slot reads pool row 0 (finite data; weight 0)
-        }
-      };
       if (my_tiles > 0) resolve(0);
       for (int jj = 0; jj < my_tiles; ++jj) {
         const uint32_t par = (jj & 1) ^ 1;  // phase of the previous tile
         const uint32_t dst = sbase + C::OFF_KV + lane * 512;
-        for (int kb = warp; kb < NB; kb += 4) {
+        for (int kb = warp; kb < NB - 1; kb += 4) {
           bad |= !mbar_wait(bar_empty(kb), par, abort_flag, p.err);
           if (kb == 0) {
             // block 0 is released by the first MMA group of the previous PV,
@@ -316,11 +326,14 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) valid_s[4 * lane + k] = v4[k];
             mbar_arrive(bar_valid);
-            // one arrival with the first part's bytes opens its phase; blocks of
-            // other warps may land before it (the count goes negative)
-            if (lane == 0) mbar_arrive_expect_tx(bar_full(0), NB_A * kBlk);
+            // one arrival with each part's bytes opens its phase; blocks of other
+            // warps may land before it (the count goes negative).  Block 0 is
+            // released after the previous S^T, so both previous phases are done.
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bar_full(0), NB_A * kBlk);
+              mbar_arrive_expect_tx(bar_full(1), (NB - NB_A) * kBlk);
+            }
           }
-          if (kb == NB - 1 && lane == 0) mbar_arrive_expect_tx(bar_full(1), (NB - NB_A) * kBlk);
           __syncwarp();
           const uint32_t bar = bar_full(kb < NB_A ? 0 : 1);
           if (!bad) tma_gather4(dst + kb * kBlk, tm_c, bar, kb * 64, r4[0], r4[1], r4[2], r4[3]);
@@ -403,6 +416,10 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       const int srow = quad * 32 + lane;  // key of S^T held by this lane
       const float c = L.scale * kLog2e;
       const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+      if (my_tiles > 0) {
+        resolve(0);
+        gather_last_block();
+      }
       float lsum[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) lsum[i] = 0.f;
@@ -493,6 +510,12 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_p_full);
+        if (jj + 1 < my_tiles) {
+          // the next tile's block NB-1 replaces this P^T once the PV has read it
+          resolve(jj + 1);
+          bad |= !mbar_wait(bar_empty(NB - 1), jj & 1, abort_flag, p.err);
+          if (!bad) gather_last_block();
+        }
       }
       // l per head over this block's keys
       red_s[quad * 64 + h0 + lane] = transpose_reduce32<false>(lsum, lane);
