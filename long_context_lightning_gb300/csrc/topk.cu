@@ -10,10 +10,10 @@
 // shared-memory histogram per block, summed across the cluster through
 // distributed shared memory.  Each block then knows how many of its keys are
 // above the threshold and how many equal it; equal keys are granted to the
-// lowest positions first.  The ordered write is per warp: each warp owns a
-// contiguous range of the chunk and places its selections with ballots, after
-// one 32-entry scan of the warps' counts.  When the chunk fits in shared
-// memory the row is read from global memory exactly once.
+// lowest positions first.  The ordered write is per thread: each thread owns
+// a contiguous run of the chunk and places its selections after one block scan
+// of the threads' counts.  When the chunk fits in shared memory the row is read
+// from global memory exactly once.
 #include "internal.cuh"
 
 namespace dsa {
@@ -52,12 +52,6 @@ __device__ __forceinline__ int warp_excl_scan(int v) {
     if (lane >= o) x += y;
   }
   return x - v;
-}
-
-__device__ __forceinline__ int warp_sum(int v) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 
 __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active) {
@@ -220,72 +214,93 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   }
   const int take = (int)min(local_equal, rem > eq_before ? rem - eq_before : 0u);
 
-  // ---- ordered write: warp w owns the contiguous range [w0, w1) of the chunk.
-  // One counting pass records per lane which of its keys are above / equal to
-  // the threshold as bits (up to 64 keys per lane), so the ordered pass needs
-  // no second read of the keys.
-  const int pw = ((len + kWarps - 1) / kWarps + 31) & ~31;
-  const int w0 = min(len, warp * pw), w1 = min(len, w0 + pw);
-  const int iters = (w1 - w0 + 31) / 32;
-  const bool in_regs = iters <= 64;
-  auto key_at = [&](int i) -> uint32_t { return cached ? cache[i] : ordered_key(row[c0 + i]); };
-  uint32_t gt_lo = 0, gt_hi = 0, eq_lo = 0, eq_hi = 0;
-  {
-    int gt = 0, eq = 0;
-    for (int it = 0; it < iters; ++it) {
-      const int i = w0 + it * 32 + lane;
-      const uint32_t key = i < w1 ? key_at(i) : 0u;
-      const uint32_t g = (i < w1 && key > thr), e = (i < w1 && key == thr);
+  // ---- ordered write: thread t owns the contiguous run [t*R, t*R + R) of the
+  // chunk (R a multiple of four, so keys are read four at a time).  A counting
+  // pass records which of its keys are above / equal to the threshold as bits
+  // (runs up to 64 keys), one block scan of the two counts places every
+  // thread's first selection, and each thread writes its own selections in
+  // position order.  Equal keys go to the lowest positions: those a thread
+  // may take are what is left of the block's allowance after the threads
+  // before it.
+  const int R = ((len + kThreads - 1) / kThreads + 3) & ~3;
+  const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
+  const bool in_regs = R <= 64;
+  auto keys4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4, i < len)
+    if (cached) {
+      const uint4 q = *reinterpret_cast<const uint4*>(cache + i);  // within the cache: len <= its 4-aligned size
+      kk[0] = q.x; kk[1] = q.y; kk[2] = q.z; kk[3] = q.w;
+    } else if (c0 + i + 3 < c1) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + c0 + i));
+      kk[0] = ordered_key(f.x); kk[1] = ordered_key(f.y); kk[2] = ordered_key(f.z); kk[3] = ordered_key(f.w);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kk[j] = (c0 + i + j < c1) ? ordered_key(row[c0 + i + j]) : 0u;
+    }
+  };
+  uint64_t gtb = 0, eqb = 0;
+  int gt = 0, eq = 0;
+  for (int i = r0; i < r1; i += 4) {
+    uint32_t kk[4];
+    keys4(i, kk);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool in = i + j < r1;
+      const bool g = in && kk[j] > thr, e = in && kk[j] == thr;
       gt += g;
       eq += e;
       if (in_regs) {
-        if (it < 32) { gt_lo |= g << it; eq_lo |= e << it; }
-        else { gt_hi |= g << (it - 32); eq_hi |= e << (it - 32); }
+        gtb |= (uint64_t)g << (i - r0 + j);
+        eqb |= (uint64_t)e << (i - r0 + j);
       }
     }
-    gt = warp_sum(gt);
-    eq = warp_sum(eq);
-    if (lane == 0) {
-      w_gt[warp] = gt;
-      w_eq[warp] = eq;
-    }
+  }
+  // block-exclusive scans of (above, equal) counts: lanes, then warps
+  const int gt_ex = warp_excl_scan(gt), eq_ex = warp_excl_scan(eq);
+  if (lane == 31) {
+    w_gt[warp] = gt_ex + gt;
+    w_eq[warp] = eq_ex + eq;
   }
   __syncthreads();
   if (warp == 0) {
-    const int e = w_eq[lane];
-    const int eb = warp_excl_scan(e);
-    const int tk = max(0, min(e, take - eb));
-    const int sb = warp_excl_scan(w_gt[lane] + tk);
-    w_eqb[lane] = eb;
-    w_selb[lane] = sb;
+    w_selb[lane] = warp_excl_scan(w_gt[lane]);
+    w_eqb[lane] = warp_excl_scan(w_eq[lane]);
   }
   __syncthreads();
   {
-    int eq_run = w_eqb[warp];
-    int pos_run = (int)base + w_selb[warp];
-    const unsigned lt = (1u << lane) - 1u;
-    for (int it = 0; it < iters; ++it) {
-      const int i = w0 + it * 32 + lane;
-      bool gtf, eqf;
-      if (in_regs) {
-        const uint32_t gw = it < 32 ? gt_lo : gt_hi, ew = it < 32 ? eq_lo : eq_hi;
-        const int sh = it & 31;
-        gtf = (gw >> sh) & 1u;
-        eqf = (ew >> sh) & 1u;
-      } else {
-        const uint32_t key = i < w1 ? key_at(i) : 0u;
-        gtf = i < w1 && key > thr;
-        eqf = i < w1 && key == thr;
+    const int gt_before = w_selb[warp] + gt_ex, eq_before_t = w_eqb[warp] + eq_ex;
+    const int allow = max(0, min(eq, take - eq_before_t));  // this thread's equal keys that are taken
+    int pos = (int)base + gt_before + min(eq_before_t, take);
+    if (in_regs) {
+      // the first `allow` equal keys, then every selection in position order
+      uint64_t eqa = 0, em = eqb;
+      for (int a = 0; a < allow; ++a) {
+        const uint64_t low = em & (~em + 1);
+        eqa |= low;
+        em ^= low;
       }
-      const unsigned eqm = __ballot_sync(0xffffffffu, eqf);
-      const bool sel = gtf || (eqf && eq_run + __popc(eqm & lt) < take);
-      const unsigned selm = __ballot_sync(0xffffffffu, sel);
-      if (sel) {
-        const int pos = pos_run + __popc(selm & lt);
-        if (pos < k) out[pos] = c0 + i;
+      uint64_t sel = gtb | eqa;
+      while (sel) {
+        const int j = __ffsll((long long)sel) - 1;
+        sel &= sel - 1;
+        if (pos < k) out[pos] = c0 + r0 + j;
+        ++pos;
       }
-      eq_run += __popc(eqm);
-      pos_run += __popc(selm);
+    } else {
+      int eq_seen = 0;
+      for (int i = r0; i < r1; i += 4) {
+        uint32_t kk[4];
+        keys4(i, kk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (i + j >= r1) continue;
+          const bool e = kk[j] == thr;
+          if (kk[j] > thr || (e && eq_seen < allow)) {
+            if (pos < k) out[pos] = c0 + i + j;
+            ++pos;
+          }
+          eq_seen += e;
+        }
+      }
     }
   }
   cluster_sync();  // peers may still read this block's shared memory
