@@ -92,6 +92,18 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
 
   for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) hist[i] = 0;
   __syncthreads();
+  auto keys4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4, i < len)
+    if (cached) {
+      const uint4 q = *reinterpret_cast<const uint4*>(cache + i);  // within the cache: len <= its 4-aligned size
+      kk[0] = q.x; kk[1] = q.y; kk[2] = q.z; kk[3] = q.w;
+    } else if (c0 + i + 3 < c1) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(row + c0 + i));
+      kk[0] = ordered_key(f.x); kk[1] = ordered_key(f.y); kk[2] = ordered_key(f.z); kk[3] = ordered_key(f.w);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kk[j] = (c0 + i + j < c1) ? ordered_key(row[c0 + i + j]) : 0u;
+    }
+  };
 
   uint32_t prefix = 0;   // digits fixed so far
   uint32_t rem = k;      // how many keys still to take at/below the current prefix
@@ -134,11 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
         }
       }
     } else {
-      for (int i0 = 0; i0 < len; i0 += kThreads) {
-        const int i = i0 + threadIdx.x;
-        const bool in = i < len;
-        const uint32_t key = in ? (cached ? cache[i] : ordered_key(row[c0 + i])) : 0u;
-        hist_add(h, (key >> sh) & msk, in && (key >> psh) == prefix);
+      for (int i = (int)threadIdx.x * 4; i < len; i += kThreads * 4) {  // four keys per step
+        uint32_t kk[4];
+        keys4(i, kk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) hist_add(h, (kk[j] >> sh) & msk, i + j < len && (kk[j] >> psh) == prefix);
       }
     }
     cluster_sync();  // every block's histogram of this digit is complete
@@ -151,15 +163,29 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     const int bpt = nb / kThreads;  // 2 or 1 bins per thread
     const int top = nb - 1 - (int)threadIdx.x * bpt;
     int tot_mine = 0, own_mine = 0;
-    for (int j = 0; j < bpt; ++j) {
-      const int bin = top - j;
-      uint32_t sum = h[bin];
-      const uint32_t local = smem_u32(h + bin);
+    if (bpt == 2) {
+      // the thread's two bins are adjacent and 8-byte aligned: one remote load per peer
+      const int b0 = top - 1;
+      uint32_t s0 = h[b0], s1 = h[b0 + 1];
+      const uint32_t local = smem_u32(h + b0);
+      for (uint32_t r = 0; r < csize; ++r)
+        if (r != crank) {
+          const uint2 v = ld_dsmem_v2_u32(dsmem_addr(local, r));
+          s0 += v.x;
+          s1 += v.y;
+        }
+      tot[b0] = s0;
+      tot[b0 + 1] = s1;
+      tot_mine = (int)(s0 + s1);
+      own_mine = (int)(h[b0] + h[b0 + 1]);
+    } else {
+      uint32_t sum = h[top];
+      const uint32_t local = smem_u32(h + top);
       for (uint32_t r = 0; r < csize; ++r)
         if (r != crank) sum += ld_dsmem_u32(dsmem_addr(local, r));
-      tot[bin] = sum;
-      tot_mine += (int)sum;
-      own_mine += (int)h[bin];
+      tot[top] = sum;
+      tot_mine = (int)sum;
+      own_mine = (int)h[top];
     }
     const int tot_ex = warp_excl_scan(tot_mine), own_ex = warp_excl_scan(own_mine);
     if (lane == 31) {
@@ -225,18 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   const int R = ((len + kThreads - 1) / kThreads + 3) & ~3;
   const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
   const bool in_regs = R <= 64;
-  auto keys4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4, i < len)
-    if (cached) {
-      const uint4 q = *reinterpret_cast<const uint4*>(cache + i);  // within the cache: len <= its 4-aligned size
-      kk[0] = q.x; kk[1] = q.y; kk[2] = q.z; kk[3] = q.w;
-    } else if (c0 + i + 3 < c1) {
-      const float4 f = __ldg(reinterpret_cast<const float4*>(row + c0 + i));
-      kk[0] = ordered_key(f.x); kk[1] = ordered_key(f.y); kk[2] = ordered_key(f.z); kk[3] = ordered_key(f.w);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) kk[j] = (c0 + i + j < c1) ? ordered_key(row[c0 + i + j]) : 0u;
-    }
-  };
   uint64_t gtb = 0, eqb = 0;
   int gt = 0, eq = 0;
   for (int i = r0; i < r1; i += 4) {
