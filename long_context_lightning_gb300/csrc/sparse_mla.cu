@@ -589,6 +589,9 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       }
       bool ok = true;
       if (csize > 1) ok = mbar_wait_cluster(bar_recv, 0, p.err);  // every source's slab has landed
+      // every peer's copy out of its staging area has completed: a peer may
+      // leave once all blocks have passed this point (the wait is at the end)
+      if (csize > 1) cluster_arrive();
       // weight of each source per head: four threads per head, each with the
       // sources sub and sub + 4; max and sum over a head's sources by shuffles
       {
@@ -650,7 +653,11 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   run_tiles();
   combine();
   // no block may leave while a peer's copy could still read its staging area
-  if (csize > 1) cluster_sync();
+  // (the softmax warps arrived after their slabs landed, the others here)
+  if (csize > 1) {
+    if (warp < 5) cluster_arrive();
+    cluster_wait();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 4) {

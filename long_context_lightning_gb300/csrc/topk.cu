@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     eq_before += e;
   }
   const int take = (int)min(local_equal, rem > eq_before ? rem - eq_before : 0u);
+  // the last remote reads are done: a block may leave once every peer has
+  // also passed this point (the wait is at the end)
+  cluster_arrive();
 
   // ---- ordered write: thread t owns the contiguous run [t*R, t*R + R) of the
   // chunk (R a multiple of four, so keys are read four at a time).  A counting
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
       }
     }
   }
-  cluster_sync();  // peers may still read this block's shared memory
+  cluster_wait();  // peers may still read this block's shared memory until they arrive
 }
 
 int g_max_cluster = 0;  // largest cluster size the device schedules for this kernel
