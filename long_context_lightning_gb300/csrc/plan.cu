@@ -9,7 +9,7 @@ namespace dsa {
 
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;  // the most threads; a small batch is planned by fewer
 constexpr int kMaxSeqs = 16384;  // cu_seqlens, lengths and group offsets kept in shared memory
 
 // Exclusive block-wide scan of one int per thread; returns the prefix and
@@ -25,7 +25,7 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sums[lane];
+    int s = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, s, o);
@@ -63,7 +63,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   const int G = p.group;
   pdl_trigger();  // the indexer's prologue may start; it waits for this grid before reading the plan
 
-  for (int i = threadIdx.x; i <= p.B; i += kPlanThreads) {
+  const int nt = blockDim.x;
+  for (int i = threadIdx.x; i <= p.B; i += nt) {
     cu_s[i] = __ldg(p.cu_seqlens_q + i);
     if (i < p.B) len_s[i] = __ldg(p.seq_lens_k + i);
   }
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 
   // (1) groups per sequence, and their offsets
   int running = 0;
-  for (int b0 = 0; b0 < p.B; b0 += kPlanThreads) {
+  for (int b0 = 0; b0 < p.B; b0 += nt) {
     const int b = b0 + threadIdx.x;
     int ng = 0;
     if (b < p.B) {
@@ -93,7 +94,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
   __syncthreads();
 
   // (2) every query: its sequence and causal context length
-  for (int t = threadIdx.x; t < p.T; t += kPlanThreads) {
+  for (int t = threadIdx.x; t < p.T; t += nt) {
     int lo = 0, hi = p.B - 1;  // last b with cu[b] <= t
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
 
   // (3) every group: its queries and its number of 128-key work items
   running = 0;
-  for (int g0 = 0; g0 < n_groups; g0 += kPlanThreads) {
+  for (int g0 = 0; g0 < n_groups; g0 += nt) {
     const int g = g0 + threadIdx.x;
     int items = 0;
     if (g < n_groups) {
@@ -148,7 +149,11 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  plan_kernel<<<1, kPlanThreads, smem, stream>>>(p);
+  // one thread per sequence or query up to the block's limit: a small batch
+  // pays barriers and scans of a few warps, not of 32
+  const int need = std::max(p.B + 1, p.T);
+  const int threads = std::min(kPlanThreads, std::max(32, (need + 31) / 32 * 32));
+  plan_kernel<<<1, threads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
