@@ -9,11 +9,15 @@
 //
 // Row gather.  The selected rows of a query are taken 128 at a time into one
 // tile of shared memory, D/64 column blocks of [128 rows x 64 dims] (128-byte
-// swizzle), by TMA tile::gather4 (four rows x 64 dims per instruction).  The
-// issue rate of these copies caps a block, so all four gather warps issue:
-// warp w owns the column blocks w, w+4, w+8.  Each column block is refilled as
-// soon as the PV MMAs that read it complete, so the next tile's copies overlap
-// the end of this tile's PV.
+// swizzle), by TMA tile::gather4 (four rows x 64 dims per instruction).  A
+// gather4 costs its warp ~30 ns (lanes in series), so the copies are spread:
+// gather warp w owns the column blocks w and w+4, and the last block (it holds
+// P^T during the PV, so it is freed last) is gathered by the eight softmax
+// warps, idle at that point.  Each column block is refilled as soon as the PV
+// MMAs that read it complete, so the next tile's copies overlap the end of
+// this tile's PV; and once a tile has landed, the next tile's rows are
+// bulk-prefetched into L2 (HBM is otherwise idle while a tile is consumed), so
+// those copies read L2.
 //
 // Tensor cores.  The same tile serves two MMAs:
 //   S^T[key, h] = C[key, :] . Q[h, :]^T     M = 128 keys, N = 64 heads, K = D
@@ -35,16 +39,18 @@
 // Split over a cluster: the selected rows of one query are divided among the
 // blocks of a thread-block cluster; each block keeps its partial (m, l, O).
 // Combine: every block writes its unnormalised partial O^T as bf16 rows
-// [value dim][head] with its (m, l) per head in front, one slab per owner of
-// a value slice; once the owner reports its tile memory free, the slab moves
-// there with one bulk copy (shared::cta -> shared::cluster), and the owner
-// weights and sums the slabs of its slice.  One exchange, no global traffic.
+// [head pair][value dim] with its (m, l) per head in front, one slab per owner
+// of a value slice; once the owner reports its tile memory free, the slab
+// moves there with one bulk copy (shared::cta -> shared::cluster), and the
+// owner weights and sums the slabs of its slice.  One exchange, no global
+// traffic.
 //
 // Warp roles (416 threads, one block per SM):
-//   warps 0..3   row gather (index -> pool row, paged or contiguous)
+//   warps 0..3   row gather (index -> pool row, paged or contiguous) of the
+//                column blocks before the last; next tile's L2 prefetch
 //   warp 4       TMEM owner, query TMA, MMA issuer (one thread)
 //   warps 5..12  softmax: two warps per TMEM lane quadrant, 32 heads each;
-//                then the combine
+//                the last column block's gather; then the combine
 #include <algorithm>
 
 #include "internal.cuh"
