@@ -11,6 +11,13 @@ Metric: query tokens/s, whole job (all ranks).
 project has) on a bounded sample of the same workload.
 Under torchrun each rank runs its own 32-sequence batch (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
+
+Beside the decode headline, the line carries `per_config`: the tiny,
+chunked-prefill, ragged-paged and IndexShare workloads, each timed the same
+way (CUDA-graph replay of the fused call, CUDA events on the launching stream,
+L2 flushed between steps) with its dominant kernel's roofline and the oracle
+timed on a bounded sample beside it.  For IndexShare one query token is one
+query through the whole 4-layer group.
 """
 from __future__ import annotations
 
@@ -35,15 +42,6 @@ import dsa_workloads as W  # noqa: E402
 
 METRIC = "DSA query tokens/s (indexer+top-k+sparse MLA) at k=2048; % HBM roofline"
 WORKLOAD = "decode"
-
-
-def _peaks():
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            p = json.load(f)
-        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
-    except Exception:
-        return 6800.0, 1900.0, "fallback"
 
 
 def _config(spec):
@@ -169,32 +167,175 @@ def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: fl
     return units_per_rank * world * steps / (max_total_ms / 1e3)
 
 
-def _traffic_from_profile(kernel_file: str, summary: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
-    path = os.path.join(ROOT, "profiles", summary)
-    src = os.path.join(ROOT, "long_context_lightning_gb300", "csrc", kernel_file)
-    try:
-        with open(src, "rb") as f:
-            h = hashlib.sha256(f.read()).hexdigest()[:16]
-        with open(path) as f:
-            txt = f.read()
-        vals = {}
-        for line in txt.splitlines():
-            if ":" in line and line.strip().startswith("- "):
-                k, v = line.strip()[2:].split(":", 1)
-                vals[k.strip()] = v.strip()
-        if vals.get("source_sha256_16") != h:
-            return None
-        return float(vals["dram_bytes_per_launch"])
-    except Exception:
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a
+# kernel from one ncu capture, keyed by workload and kernel, with the first 16
+# hex digits of the sha256 of the kernel's source file when it was captured.
+# A source that has changed since makes the figure stale: it is reported as
+# null.  Captured with
+#   ncu --set full --clock-control none -k regex:<kernel>_kernel -s 2 -c 1 \
+#       -o <report> python bench.py --steps 5 --warmup 3
+NCU_TRAFFIC = {
+    ("decode", "indexer"): ("indexer.cu", "f2c2c4f582978c1a", 275527424.0),
+}
+
+
+def _traffic(workload: str, kernel: str):
+    entry = NCU_TRAFFIC.get((workload, kernel))
+    if entry is None:
         return None
+    src, sha, nbytes = entry
+    try:
+        with open(os.path.join(ROOT, "long_context_lightning_gb300", "csrc", src), "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return nbytes if h == sha else None
+
+
+def _peaks_all():
+    """HBM copy GB/s, bf16 TFLOP/s burst and sustained, and where they come from."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return (float(p["hbm_gbs"]), float(p["bf16_tflops"]),
+                float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured")
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+KERNELS = ("plan", "indexer", "topk", "sparse_mla")
+
+
+class _Run:
+    """One workload resident on the device, its fused call captured in a CUDA graph."""
+
+    def __init__(self, spec, dev):
+        from long_context_lightning_gb300 import _lib
+        from long_context_lightning_gb300.api import SparseAttention
+        self.spec = spec
+        self.dev = dev
+        self.wl = W.make_workload(spec, device=dev)
+        wl = self.wl
+        self.sa = SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, spec.d_v,
+                                  spec.scale, spec.topk, seq_start=wl.seq_start, page_table=wl.page_table,
+                                  page_size=spec.page_size)
+        self.sa.forward()
+        torch.cuda.synchronize(dev)
+        status = _lib.check_device_error()
+        if status != _lib.DSA_OK:
+            raise RuntimeError(f"{spec.name}: device error after the first forward: {_lib.status_string(status)}")
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, capture_error_mode="thread_local"):
+            self.sa.forward()
+        torch.cuda.synchronize(dev)
+
+    def time_steps(self, steps, warmup, flush_l2, stream, settle_s=0.0):
+        """CUDA-event time of each of `steps` graph replays, L2 flushed before each (outside the events)."""
+        for _ in range(max(warmup, 3)):
+            self.graph.replay()
+        t_busy = time.perf_counter()
+        while time.perf_counter() - t_busy < settle_s:
+            for _ in range(50):
+                self.graph.replay()
+            torch.cuda.synchronize(self.dev)
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        torch.cuda.synchronize(self.dev)
+        for i in range(steps):
+            flush_l2(i)
+            starts[i].record(stream)
+            self.graph.replay()
+            ends[i].record(stream)
+        torch.cuda.synchronize(self.dev)
+        return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+    def kernel_ms(self, n, flush_l2, stream):
+        """Mean time of each launch from a separate run of dsa_forward_marked (events between the launches;
+        the marks stop programmatic overlap, so the means add up to more than a step)."""
+        from long_context_lightning_gb300 import _lib
+        sa = self.sa
+        marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
+        for row in marks:          # torch creates the CUDA event on first record
+            for m in row:
+                m.record(stream)
+        torch.cuda.synchronize(self.dev)
+        for i in range(n):
+            flush_l2(i)
+            _lib.forward_marked(sa.batch, sa.indexer, sa.topk, sa.layers, sa.idx, sa.outs, sa.lses, sa.workspace,
+                                marks[i])
+        torch.cuda.synchronize(self.dev)
+        per = {k: [] for k in KERNELS}
+        for m in marks:
+            for j, name in enumerate(KERNELS):
+                per[name].append(m[j].elapsed_time(m[j + 1]))
+        return {k: statistics.mean(v) for k, v in per.items()}
+
+    def check(self, what):
+        from long_context_lightning_gb300 import _lib
+        status = _lib.check_device_error()
+        if status != _lib.DSA_OK:
+            raise RuntimeError(f"{what}: device error: {_lib.status_string(status)}")
+
+
+def _roofline(wl, kern_ms, peaks, workload):
+    """Dominant kernel's roofline (HBM bytes or tensor FLOPs, algorithmic), plus the sparse MLA's and the
+    whole step's byte fractions."""
+    from long_context_lightning_gb300 import accounting as A
+    hbm, tf_burst, tf_sust, kind = peaks
+    shp = _shape(wl)
+    work = {
+        "indexer": (A.indexer_bytes(shp), A.indexer_flops(shp)),
+        "topk": (A.topk_bytes(shp), 0),
+        "sparse_mla": (A.mla_bytes(shp), A.mla_flops(shp)),
+    }
+    dom = max(("indexer", "topk", "sparse_mla"), key=lambda k: kern_ms[k])
+    nbytes, flops = work[dom]
+    sec = kern_ms[dom] * 1e-3
+    # a kernel whose FLOPs per byte exceed the ridge of the measured peaks is tensor-bound
+    ridge = tf_sust * 1e12 / (hbm * 1e9)
+    if flops and flops / max(nbytes, 1) > ridge:
+        ach = flops / sec / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_sust, "unit": "TFLOP/s",
+                "frac": ach / tf_sust, "traffic": _traffic(workload, dom), "peak_kind": f"{kind} (bf16 sustained)",
+                "algorithmic_flops_per_launch": flops}
+    else:
+        ach = nbytes / sec / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                "traffic": _traffic(workload, dom), "peak_kind": kind, "algorithmic_bytes_per_launch": nbytes}
+    mla_b, mla_f = work["sparse_mla"]
+    mla_gbs = mla_b / (kern_ms["sparse_mla"] * 1e-3) / 1e9
+    mla = {"bound": "hbm", "achieved": mla_gbs, "peak": hbm, "unit": "GB/s", "frac": mla_gbs / hbm,
+           "traffic": _traffic(workload, "sparse_mla"), "algorithmic_bytes_per_launch": mla_b,
+           "tflops": mla_f / (kern_ms["sparse_mla"] * 1e-3) / 1e12}
+    return roof, mla, A.forward_bytes(shp), A.forward_flops(shp)
+
+
+def _oracle_sample(wl, queries, kv_on_device=False):
+    """The oracle as it stands over `queries` of a workload; (seconds, queries done)."""
+    import oracle
+    fetch = None
+    if kv_on_device:
+        fetch = lambda layer, rows: wl.kv[layer][torch.from_numpy(rows).to(wl.kv[layer].device)].cpu()  # noqa: E731
+        cpu = wl.to("cpu", kv_too=False)
+    else:
+        cpu = wl.to("cpu")
+    t0 = time.perf_counter()
+    oracle.dsa_forward(cpu, queries=queries, kv_rows_fetch=fetch)
+    return time.perf_counter() - t0, len(queries)
+
+
+# per workload: which queries the CPU baseline times (a bounded sample, a few seconds each)
+CPU_SAMPLE = {
+    "tiny": (lambda T: list(range(T)), "all 16 queries"),
+    "prefill": (lambda T: [0, T // 2, T - 1], "3 of the 4096 chunk queries (first, middle, last)"),
+    "ragged": (lambda T: list(range(0, T, 4)), "every 4th of the 64 ragged queries"),
+    "indexshare": (lambda T: [0], "1 of the 2 queries, through all 4 layers"),
+}
 
 
 def run_gpu(args, rank, world, local_rank):
     import __graft_entry__
     from long_context_lightning_gb300 import _lib
-    from long_context_lightning_gb300 import accounting
-    from long_context_lightning_gb300.api import SparseAttention
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -203,23 +344,9 @@ def run_gpu(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     _lib.load()
-    spec = W.SPECS[WORKLOAD].scaled(seed=W.SPECS[WORKLOAD].seed + 100 * rank)
-    wl = W.make_workload(spec, device=dev)
-    sa = SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, spec.d_v,
-                         spec.scale, spec.topk, seq_start=wl.seq_start)
     stream = torch.cuda.current_stream(dev)
-    sa.forward()
-    torch.cuda.synchronize(dev)
-    status = _lib.check_device_error()
-    if status != _lib.DSA_OK:
-        raise RuntimeError(f"device error after the first forward: {_lib.status_string(status)}")
-
-    # one forward captured in a CUDA graph (4 launches: plan, indexer, top-k, sparse MLA)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-        sa.forward()
-    torch.cuda.synchronize(dev)
-    launches_per_step = 4
+    peaks = _peaks_all()
+    hbm = peaks[0]
 
     # L2 flush between timed steps: write 512 MB (> the 129 MB L2), then read a
     # 256 MB buffer so the lines left in L2 are clean (no write-back lands in
@@ -230,53 +357,25 @@ def run_gpu(args, rank, world, local_rank):
     def flush_l2(i):
         flush.fill_(i)
         scrub.sum()
+
+    spec = W.SPECS[WORKLOAD].scaled(seed=W.SPECS[WORKLOAD].seed + 100 * rank)
+    run = _Run(spec, dev)
+    wl, sa = run.wl, run.sa
+    launches_per_step = 4      # plan, indexer, top-k, sparse MLA
+
     clocks = ClockSampler(dev)
     clocks.start()
-    # warm-up: W graph replays, then enough extra replays for the clocks to settle under load
-    for _ in range(max(args.warmup, 3)):
-        graph.replay()
-    t_busy = time.perf_counter()
-    while time.perf_counter() - t_busy < 0.5:
-        for _ in range(50):
-            graph.replay()
-        torch.cuda.synchronize(dev)
-
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2(i)                         # between timed steps, outside the events
-        starts[i].record(stream)
-        graph.replay()
-        ends[i].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms = run.time_steps(args.steps, args.warmup, flush_l2, stream, settle_s=0.5)
     wall = time.perf_counter() - wall0
     if world > 1:
         torch.distributed.barrier()
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = sum(step_ms)
-
-    # per-kernel times on the same stream (marks between the launches), same flushing
-    n_brk = min(args.steps, 200)
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_brk)]
-    for row in marks:          # torch creates the CUDA event on first record
-        for m in row:
-            m.record(stream)
-    torch.cuda.synchronize(dev)
-    for i in range(n_brk):
-        flush_l2(i)
-        _lib.forward_marked(sa.batch, sa.indexer, sa.topk, sa.layers, sa.idx, sa.outs, sa.lses, sa.workspace,
-                            marks[i])
-    torch.cuda.synchronize(dev)
+    kern_ms = run.kernel_ms(min(args.steps, 200), flush_l2, stream)
     clk = clocks.stop()
-    per = {"plan": [], "indexer": [], "topk": [], "sparse_mla": []}
-    for m in marks:
-        for j, name in enumerate(per):
-            per[name].append(m[j].elapsed_time(m[j + 1]))
-    kern_ms = {k: statistics.mean(v) for k, v in per.items()}
 
     # end to end through the public API: inputs from pinned host memory, results back
     host_in = [t.cpu().pin_memory() for t in
@@ -306,26 +405,25 @@ def run_gpu(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / n_e2e
-    status = _lib.check_device_error()
-    if status != _lib.DSA_OK:
-        raise RuntimeError(f"device error during the benchmark: {_lib.status_string(status)}")
+    run.check("decode benchmark")
 
     # aggregate over ranks: max time
     T = wl.total_q
     total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dev)
+    roof, mla_roof, all_bytes, _ = _roofline(wl, kern_ms, peaks, WORKLOAD)
+    wl_cpu = wl.to("cpu")
+    del run, sa, host_in, host_out
     if rank != 0:
         return
     value = job_throughput(T, world, args.steps, total_ms)
-    hbm, tf, peak_kind = _peaks()
-    shp = _shape(wl)
-    idx_bytes = accounting.indexer_bytes(shp)
-    mla_bytes = accounting.mla_bytes(shp)
-    all_bytes = accounting.forward_bytes(shp)
-    idx_gbs = idx_bytes / (kern_ms["indexer"] * 1e-3) / 1e9
-    mla_gbs = mla_bytes / (kern_ms["sparse_mla"] * 1e-3) / 1e9
-    traffic = _traffic_from_profile("indexer.cu", "indexer_decode_b32_ctx32k.md")
-    wl_cpu = wl.to("cpu")
-    cpu = _cpu_baseline(spec, wl_cpu) if world == 1 or rank == 0 else None
+    cpu = _cpu_baseline(spec, wl_cpu, budget_s=8.0) if world == 1 or rank == 0 else None
+    del wl_cpu
+
+    # the other workloads: parity cases, timed the same way (rank 0 only, one GPU)
+    per_config = {}
+    if not args.no_per_config:
+        per_config = _per_config(args, dev, stream, flush_l2, peaks)
+
     line = {
         "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -333,12 +431,12 @@ def run_gpu(args, rank, world, local_rank):
         "config": {**_config(spec), "parallelism": f"dp{world} (independent batches per GPU)",
                    "l2": "flushed between timed steps (512 MB write + 256 MB read, outside the timed events)",
                    "cuda_graph": True},
-        "roofline": {"bound": "hbm", "kernel": "indexer", "achieved": idx_gbs, "peak": hbm, "unit": "GB/s",
-                     "frac": idx_gbs / hbm, "traffic": traffic, "peak_kind": peak_kind,
-                     "algorithmic_bytes_per_launch": idx_bytes},
+        "roofline": roof,
         "kernels_ms": kern_ms,
-        "sparse_mla_roofline": {"bound": "hbm", "achieved": mla_gbs, "peak": hbm, "unit": "GB/s",
-                                "frac": mla_gbs / hbm, "algorithmic_bytes_per_launch": mla_bytes},
+        "kernels_ms_source": "separate run of dsa_forward_marked: CUDA events between the four launches on the "
+                             "launching stream, L2 flushed before each call; the events stop programmatic "
+                             "overlap, so the four means add up to more than ms_per_step",
+        "sparse_mla_roofline": mla_roof,
         "step_roofline": {"bound": "hbm", "achieved": all_bytes / (total_ms / args.steps * 1e-3) / 1e9,
                           "peak": hbm, "unit": "GB/s",
                           "frac": all_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm,
@@ -349,8 +447,45 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clk,
         "wall_s_timed_region": wall,
         "cpu_baseline": cpu,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
+
+
+def _per_config(args, dev, stream, flush_l2, peaks):
+    out = {}
+    steps = max(3, min(args.steps, 20))
+    for name in ("tiny", "prefill", "ragged", "indexshare"):
+        spec = W.SPECS[name]
+        run = _Run(spec, dev)
+        step_ms = run.time_steps(steps, args.warmup, flush_l2, stream)
+        kern_ms = run.kernel_ms(steps, flush_l2, stream)
+        run.check(name)
+        wl = run.wl
+        ms = statistics.mean(step_ms)
+        T = wl.total_q
+        roof, mla_roof, all_bytes, all_flops = _roofline(wl, kern_ms, peaks, name)
+        pick, what = CPU_SAMPLE[name]
+        queries = pick(T)
+        del run
+        torch.cuda.empty_cache()
+        dt, nq = _oracle_sample(wl, queries, kv_on_device=(name == "indexshare"))
+        out[name] = {
+            "workload": _config(spec)["workload"] + (f", {spec.n_layers} layers" if spec.n_layers > 1 else "")
+                        + (", paged 64-token pages, lengths U{256..16384}" if spec.paged else ""),
+            "value": T / (ms * 1e-3), "unit": "query tokens/s" + (" (one query through the 4-layer group)"
+                                                                   if spec.n_layers > 1 else ""),
+            "ms_per_step": ms, "steps": steps, "kernels_ms": kern_ms, "roofline": roof,
+            "sparse_mla_roofline": mla_roof,
+            "step": {"algorithmic_bytes": all_bytes, "algorithmic_flops": all_flops,
+                     "hbm_frac": all_bytes / (ms * 1e-3) / 1e9 / peaks[0]},
+            "cpu_baseline": {"value": nq / dt, "unit": "query tokens/s", "kind": "oracle",
+                             "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+                             "sample": f"{what}, float64 numpy, {dt:.1f} s"},
+        }
+        del wl
+        torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -359,6 +494,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-per-config", action="store_true", help="time the decode headline only")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

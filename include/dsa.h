@@ -125,6 +125,10 @@ typedef struct {
 /* Largest supported top-k and IndexShare group. */
 #define DSA_MAX_TOPK 2048
 #define DSA_MAX_LAYERS 4
+/* Largest total_q of one call, and of total_q * n_layers for dsa_forward
+ * (one grid row per query and layer); larger batches return
+ * DSA_ERR_UNSUPPORTED: split them into several calls. */
+#define DSA_MAX_QUERIES 65535
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* dsa_status_string(dsa_status_t status);
@@ -243,6 +247,11 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  * [64, 64] row-major, D fp32 [128, 64].  `a_mn_major` / `b_mn_major` stage the
  * operand transposed (as the attention value and probability operands are).
  *
+ * dsa_selftest_topk_max_cluster: caps the thread-block cluster the top-k
+ * launches use on the current device at `max_cluster` blocks (1, 2, 4, 8 or
+ * 16; 0 restores the default), so tests can drive the paths taken when a row
+ * is split over fewer blocks (long per-thread runs).  Host state only.
+ *
  * dsa_selftest_timeout: launches one block that waits on a barrier nobody
  * arrives at; the bounded wait gives up after about `limit_ms` milliseconds
  * and sets the device error word, which dsa_check_device_error then reports
@@ -250,6 +259,7 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  */
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
                               cudaStream_t stream);
+dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster);
 dsa_status_t dsa_selftest_timeout(int32_t limit_ms, cudaStream_t stream);
 
 #ifdef __cplusplus

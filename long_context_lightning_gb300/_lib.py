@@ -22,10 +22,11 @@ DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUD
 CACHE_CONTIGUOUS, CACHE_PAGED = 0, 1
 MAX_TOPK = 2048
 MAX_LAYERS = 4
+MAX_QUERIES = 65535
 
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
-           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc"]
+           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster"]
 NOALLOC_MAX_QUERIES = 4096
 
 
@@ -93,6 +94,8 @@ def load() -> ctypes.CDLL:
                                                c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_mma.restype = c_int32
     lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p]
+    lib.dsa_selftest_topk_max_cluster.restype = c_int32
+    lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
     lib.dsa_selftest_timeout.restype = c_int32
     lib.dsa_selftest_timeout.argtypes = [c_int32, c_void_p]
     _lib = lib
@@ -227,6 +230,11 @@ def selftest_mma(a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, a_mn_major: 
                  stream=None):
     _check(load().dsa_selftest_mma(_ptr(a), _ptr(b), _ptr(d), int(a_mn_major), int(b_mn_major), _stream(stream)),
            "dsa_selftest_mma")
+
+
+def selftest_topk_max_cluster(max_cluster: int):
+    """Cap the top-k cluster size on the current device (0 restores the default)."""
+    _check(load().dsa_selftest_topk_max_cluster(max_cluster), "dsa_selftest_topk_max_cluster")
 
 
 def selftest_timeout(limit_ms: int, stream=None):

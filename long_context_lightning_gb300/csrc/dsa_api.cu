@@ -40,6 +40,11 @@ dsa_status_t device_info(DeviceInfo* out) {
   return DSA_OK;
 }
 
+// Per-device cluster-size probes of the kernels (see max_cluster_for).
+int g_cluster_max[kMaxDevices][kClusterSlots] = {};
+int g_topk_cap[kMaxDevices] = {};
+std::mutex g_cluster_mu;
+
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -54,6 +59,9 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
   if (b == nullptr) return DSA_ERR_INVALID_ARG;
   if (b->num_seqs < 1 || b->num_seqs > 16384 || b->total_q < 0 || b->max_seqlen_k < 1 || b->max_q_per_seq < 0)
     return DSA_ERR_INVALID_ARG;
+  // one grid row per query (per query and layer for the attention): the grid's
+  // y extent is at most 65535
+  if (b->total_q > DSA_MAX_QUERIES) return DSA_ERR_UNSUPPORTED;
   if (b->total_q > 0 && (b->cu_seqlens_q == nullptr || b->seq_lens_k == nullptr || !aligned4(b->cu_seqlens_q) ||
                          !aligned4(b->seq_lens_k)))
     return DSA_ERR_INVALID_ARG;
@@ -197,6 +205,42 @@ dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_l
 }
 
 }  // namespace
+
+int max_cluster_for(const void* kern, int threads, size_t smem, int slot) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kClusterSlots)
+    return 0;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  int& m = g_cluster_max[dev][slot];
+  if (m == 0) {
+    // function attributes are per device: allow non-portable sizes on this one
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
+    int best = 8;
+    cudaLaunchConfig_t probe = {};
+    probe.gridDim = dim3(16, 1, 1);
+    probe.blockDim = dim3(threads, 1, 1);
+    probe.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 16;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    probe.attrs = &at;
+    probe.numAttrs = 1;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &probe) == cudaSuccess && nclusters > 0) best = 16;
+    cudaGetLastError();  // a refused probe leaves no sticky error behind
+    m = best;
+  }
+  return m;
+}
+
+int topk_cluster_cap() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  return g_topk_cap[dev];
+}
 
 CUresult encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
@@ -412,6 +456,7 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
   if ((s = check_indexer(indexer, batch)) != DSA_OK) return s;
   if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (n_layers < 1 || n_layers > DSA_MAX_LAYERS || layers == nullptr || outs == nullptr) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)batch->total_q * n_layers > DSA_MAX_QUERIES) return DSA_ERR_UNSUPPORTED;
   for (int l = 0; l < n_layers; ++l) {
     if ((s = check_layer(&layers[l], batch)) != DSA_OK) return s;
     if (layers[l].d_qk != layers[0].d_qk || layers[l].d_v != layers[0].d_v) return DSA_ERR_UNSUPPORTED;
@@ -513,6 +558,17 @@ dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_
                                               static_cast<const __nv_bfloat16*>(b), d, a_mn_major, b_mn_major,
                                               dev.err);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster) {
+  if (max_cluster != 0 && max_cluster != 1 && max_cluster != 2 && max_cluster != 4 && max_cluster != 8 &&
+      max_cluster != 16)
+    return DSA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  g_topk_cap[dev] = max_cluster;
+  return DSA_OK;
 }
 
 dsa_status_t dsa_selftest_timeout(int32_t limit_ms, cudaStream_t stream) {

@@ -154,6 +154,16 @@ struct MlaLaunch {
 };
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
 
+// Largest thread-block cluster (8, or 16 where the device schedules it) for
+// kernel `kern` launched with `threads` threads and `smem` bytes of dynamic
+// shared memory, on the current device.  Probed once per (device, slot) under
+// a lock; non-portable sizes are enabled on that device first.  Returns 0 when
+// a CUDA call fails.  `slot` names the kernel variant (kClusterSlot*).
+enum { kClusterSlotTopk = 0, kClusterSlotMla0 = 1, kClusterSlotMla1 = 2, kClusterSlots = 4 };
+int max_cluster_for(const void* kern, int threads, size_t smem, int slot);
+// Cap on the top-k cluster size set by dsa_selftest_topk_max_cluster (0: none).
+int topk_cluster_cap();
+
 // Tensor-map encoder (driver entry point, resolved once).
 CUresult encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,
                      const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,

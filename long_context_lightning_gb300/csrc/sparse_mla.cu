@@ -672,8 +672,6 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   }
 }
 
-int g_max_cluster_mla[2] = {0, 0};
-
 template <int NB, int MB>
 cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   using C = MlaCfg<NB, MB>;
@@ -701,30 +699,13 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  if (g_max_cluster_mla[which] == 0) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    g_max_cluster_mla[which] = 8;
-    cudaLaunchConfig_t probe = {};
-    probe.gridDim = dim3(16, 1, 1);
-    probe.blockDim = dim3(C::THREADS, 1, 1);
-    probe.dynamicSmemBytes = C::SMEM_BYTES;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = 16;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    probe.attrs = &at;
-    probe.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &probe) == cudaSuccess && nclusters > 0)
-      g_max_cluster_mla[which] = 16;
-    cudaGetLastError();
-  }
+  const int max_cluster = max_cluster_for(reinterpret_cast<const void*>(kern), C::THREADS, C::SMEM_BYTES,
+                                          which == 0 ? kClusterSlotMla0 : kClusterSlotMla1);
+  if (max_cluster == 0) return cudaErrorUnknown;
   const int units = a.T * a.n_layers;
   const int tiles_max = (std::min(a.k, a.max_n) + kRows - 1) / kRows;
   int c = 1;
-  while (c * 2 <= std::min(g_max_cluster_mla[which], kMaxSplit) && c * 2 <= tiles_max &&
+  while (c * 2 <= std::min(max_cluster, kMaxSplit) && c * 2 <= tiles_max &&
          (int64_t)units * c * 2 <= a.num_sms)
     c *= 2;
   // every block owns a value slice of >= 32 dims (one warp's lanes write one owner's slab)

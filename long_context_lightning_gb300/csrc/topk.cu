@@ -14,6 +14,8 @@
 // a contiguous run of the chunk and places its selections after one block scan
 // of the threads' counts.  When the chunk fits in shared memory the row is read
 // from global memory exactly once.
+#include <algorithm>
+
 #include "internal.cuh"
 
 namespace dsa {
@@ -323,43 +325,26 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   cluster_wait();  // peers may still read this block's shared memory until they arrive
 }
 
-int g_max_cluster = 0;  // largest cluster size the device schedules for this kernel
-
 }  // namespace
 
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  if (g_max_cluster == 0) {
-    cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    g_max_cluster = 8;
-    cudaLaunchConfig_t probe = {};
-    probe.gridDim = dim3(16, 1, 1);
-    probe.blockDim = dim3(kThreads, 1, 1);
-    probe.dynamicSmemBytes = (4 * kBins + kMaxCacheKeys) * 4;
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)probe.dynamicSmemBytes);
-    if (e != cudaSuccess) return e;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = 16;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    probe.attrs = &at;
-    probe.numAttrs = 1;
-    int nclusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&nclusters, topk_kernel, &probe) == cudaSuccess && nclusters > 0)
-      g_max_cluster = 16;
-    cudaGetLastError();
-  }
+  const int probe_smem = (4 * kBins + kMaxCacheKeys) * 4;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, probe_smem);
+  if (e != cudaSuccess) return e;
+  int max_cluster = max_cluster_for(reinterpret_cast<const void*>(topk_kernel), kThreads, probe_smem,
+                                    kClusterSlotTopk);
+  if (max_cluster == 0) return cudaErrorUnknown;
+  if (topk_cluster_cap() > 0) max_cluster = std::min(max_cluster, topk_cluster_cap());
   // cluster size: enough blocks per row that the rows fill a good share of the
   // GPU (each block reads less of the row), and chunks that fit the key cache
   int c = 1;
-  while (c < g_max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
-  while (c < g_max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
+  while (c < max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
+  while (c < max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
   const int per = (((a.max_n + c - 1) / c) + 3) & ~3;
   const int cache_keys = per <= kMaxCacheKeys ? per : 0;
   const size_t smem = (size_t)(4 * kBins + cache_keys) * 4;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
 
   TopkParams p;

@@ -32,7 +32,7 @@ What is computed, and where it is defined:
                       ...", How it works / IndexShare: every 4 DSA layers share
                       one indexer and the top-k indices are cached for reuse).
 
-Readings where the pages are silent (each one listed in the design doc):
+Readings where the pages are silent:
   * one indexer key per token, shared by all indexer heads;
   * ReLU per head before weighting; weights unnormalised and may be negative;
   * causality includes the query's own position (n_t = p_t + 1);

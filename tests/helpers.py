@@ -4,6 +4,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import dsa_workloads as W
 import oracle
 
 OUT_MAX_REL = 1e-2    # max |err| <= 1e-2 * max |ref|
@@ -35,12 +36,28 @@ def check_lse(got: np.ndarray, ref: np.ndarray, what: str):
     np.testing.assert_allclose(got, ref, rtol=1e-4, atol=1e-4, err_msg=what)
 
 
-def judge_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=None):
+class SeqKeys:
+    """float64 indexer keys of one sequence, decoded once with the oracle's own
+    bf16 -> float64 conversion, so that many queries of that sequence are
+    scored by oracle.indexer_scores without re-reading the pool each time."""
+
+    def __init__(self, wl, b, n):
+        rows = W.pool_rows(wl, b, torch.arange(n))
+        self.b = b
+        self.keys = oracle.bf16_to_f64(wl.k_idx[rows.to(wl.k_idx.device)])
+
+    def scores(self, wl, t, n):
+        return oracle.indexer_scores(oracle.bf16_to_f64(wl.q_idx[t]), oracle.f32_to_f64(wl.w[t]), self.keys[:n])
+
+
+def judge_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=None, seq_keys=None):
     """Compare the GPU result of `queries` with the oracle.
 
     Indices: bit-exact when `exact_idx` (integer indexer inputs), else the band
     rule.  Outputs/LSE: oracle attention over the GPU's own index set, for every
     layer (near-tie swaps inside the band change attention legitimately).
+    `seq_keys` (a SeqKeys of the queries' one sequence) speeds up scoring many
+    queries of one long sequence.
     """
     spec = wl.spec
     seq, pos = wl.query_positions()
@@ -54,7 +71,10 @@ def judge_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=N
         if n <= spec.topk:
             assert np.array_equal(sel, np.arange(n)), f"query {t}: dense row"
         else:
-            s = oracle.scores_for_query(wl, t)
+            if seq_keys is not None and seq_keys.b == seq[t]:
+                s = seq_keys.scores(wl, t, n)
+            else:
+                s = oracle.scores_for_query(wl, t)
             if exact_idx:
                 assert np.array_equal(sel, oracle.topk_select(s, spec.topk)), f"query {t}: top-k differs"
             else:

@@ -2,7 +2,8 @@
 benchmark times (the same fused call, also replayed from a CUDA graph).
 
 Decode, ragged and IndexShare are judged on every query; the prefill chunk on
-a sample of queries (the oracle scores 131072 keys per query in float64).
+its first and last query plus 254 seeded ones (the oracle scores up to 131072
+keys per query in float64).
 Properties that hold at any size (ascending distinct positions inside the
 causal context, finite outputs) are checked on every row.
 """
@@ -11,7 +12,7 @@ import pytest
 import torch
 
 import dsa_workloads as W
-from helpers import judge_forward, make_sa
+from helpers import SeqKeys, judge_forward, make_sa
 
 pytestmark = pytest.mark.gpu
 
@@ -74,8 +75,10 @@ def test_prefill_full_sampled(lib):
     _rows_valid(wl, idx)
     assert torch.isfinite(outs[0].float()).all()
     rng = np.random.default_rng(2)
-    sample = sorted({0, 1, 2, 3, 4095, 4094, 2048, *rng.choice(4096, 9, replace=False).tolist()})
-    judge_forward(wl.to("cpu"), idx, outs, lses, sample)
+    sample = [0, 4095, *(1 + rng.choice(4094, 254, replace=False)).tolist()]
+    assert len(set(sample)) == 256
+    cpu = wl.to("cpu")
+    judge_forward(cpu, idx, outs, lses, sorted(sample), seq_keys=SeqKeys(cpu, 0, 131072))
 
 
 def test_ragged_paged_full(lib):

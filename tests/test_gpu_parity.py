@@ -68,9 +68,15 @@ def test_tiny_indexer_scores_exact(lib):
         assert np.all(np.isnan(got[t, pos[t] + 1:])), "entries past the causal context must stay unwritten"
 
 
-@pytest.mark.parametrize("n,k,kind", [(5000, 2048, "normal"), (3000, 2048, "ties"), (40000, 2048, "normal"),
-                                      (2000, 2048, "normal"), (700, 64, "zeros"), (1048576, 2048, "normal")])
-def test_topk_exact_on_given_scores(lib, n, k, kind):
+@pytest.mark.parametrize("n,k,kind,cap", [
+    (5000, 2048, "normal", 0), (3000, 2048, "ties", 0), (40000, 2048, "normal", 0), (2000, 2048, "normal", 0),
+    (700, 64, "zeros", 0), (1048576, 2048, "normal", 0),
+    # ties at the k-th key spread over the blocks of 16-block clusters
+    (200000, 2048, "ties2", 0), (1048576, 2048, "ties2", 0), (1048576, 2048, "ties_top", 0),
+    # clusters capped at 8 blocks: 131072 keys per block, 128-key runs per thread
+    # (the write path that re-reads its run instead of keeping bitmasks)
+    (1048576, 2048, "ties2", 8), (1048576, 2048, "normal", 8), (300000, 1000, "ties_top", 2)])
+def test_topk_exact_on_given_scores(lib, n, k, kind, cap):
     # both sides decide on the same fp32 values: the selection must match bit for bit
     g = torch.Generator().manual_seed(n + k)
     T = 3
@@ -78,6 +84,13 @@ def test_topk_exact_on_given_scores(lib, n, k, kind):
         s = torch.randn((T, n), generator=g)
     elif kind == "ties":
         s = torch.randint(-5, 6, (T, n), generator=g).float()
+    elif kind == "ties2":
+        s = torch.randint(-2, 3, (T, n), generator=g).float()
+    elif kind == "ties_top":
+        # a few hundred keys above a huge run of equal keys spread over the whole
+        # row: the equal keys taken must be the lowest positions, whichever block holds them
+        s = torch.zeros((T, n))
+        s[:, torch.randperm(n, generator=g)[:300]] = 1.0
     else:  # signed zeros and a few positives
         s = torch.zeros((T, n))
         s[:, ::3] = -0.0
@@ -91,8 +104,12 @@ def test_topk_exact_on_given_scores(lib, n, k, kind):
     batch = lib.make_batch(cu, lens, T, n, 1)
     ws = torch.empty(lib.workspace_size(batch, k), dtype=torch.uint8, device="cuda")
     idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
-    lib.topk(batch, scores, k, idx, ws)
-    assert lib.check_device_error() == lib.DSA_OK
+    lib.selftest_topk_max_cluster(cap)
+    try:
+        lib.topk(batch, scores, k, idx, ws)
+        assert lib.check_device_error() == lib.DSA_OK
+    finally:
+        lib.selftest_topk_max_cluster(0)
     got = idx.cpu().numpy()
     for t in range(T):
         ref = oracle.topk_select(s[t].double().numpy(), k)

@@ -1,9 +1,15 @@
-"""The benchmark's N-rank path on CPU ranks (gloo, world size 2): every rank
-works on its own batch (no collective on the data path); the only collective
-is the max over ranks of the timings, and the job rate counts every rank's
-units over the slowest rank's time."""
+"""The benchmark's N-rank path on CPU ranks (gloo, world size 2).
+
+Every rank works on its own seeded batch (no collective on the data path):
+here each rank runs the float64 oracle over its own tiny batch, times that
+work, and the ranks agree on the slowest rank's time with the benchmark's own
+max_over_ranks; the job rate then counts every rank's query tokens over that
+time (job_throughput).  The test checks the aggregation against the per-rank
+timings the ranks actually measured, and that the ranks' work differed.
+"""
 import os
 import socket
+import time
 
 import pytest
 import torch
@@ -24,19 +30,32 @@ def _worker(rank, world, port, out):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
     dist.init_process_group("gloo", rank=rank, world_size=world)
+    import numpy as np
+
     import bench
     import dsa_workloads as W
-    # each rank draws its own batch from a rank-specific seed
+    import oracle
+    # each rank draws its own batch from a rank-specific seed, as bench.py does
     spec = W.SPECS["tiny"].scaled(seed=W.SPECS["tiny"].seed + 100 * rank)
     wl = W.make_workload(spec)
-    local_ms = [10.0 + 5.0 * rank, 3.0 - rank]
-    mx = bench.max_over_ranks(local_ms, torch.device("cpu"))
-    out[rank] = (mx, bench.job_throughput(wl.total_q, world, 7, mx[0]), float(wl.k_idx.float().sum()))
+    steps = 2
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        res = oracle.dsa_forward(wl)
+    local_ms = (time.perf_counter() - t0) * 1e3
+    # the work is real: every query selected k positions inside its causal context
+    seq, pos = wl.query_positions()
+    for t in range(wl.total_q):
+        assert len(res.idx[t]) == spec.topk and res.idx[t].max() <= pos[t]
+    digest = float(sum(float(np.abs(res.out[0][t]).sum()) for t in range(wl.total_q)))
+    mx = bench.max_over_ranks([local_ms], torch.device("cpu"))
+    rate = bench.job_throughput(wl.total_q, world, steps, mx[0])
+    out[rank] = (local_ms, mx[0], rate, wl.total_q, steps, digest)
     dist.barrier()
     dist.destroy_process_group()
 
 
-def test_two_cpu_ranks_aggregate():
+def test_two_cpu_ranks_run_their_own_batches_and_aggregate():
     world = 2
     port = _free_port()
     mgr = mp.Manager()
@@ -46,9 +65,12 @@ def test_two_cpu_ranks_aggregate():
     for p in procs:
         p.start()
     for p in procs:
-        p.join(timeout=120)
+        p.join(timeout=300)
         assert p.exitcode == 0
-    (mx0, v0, s0), (mx1, v1, s1) = out[0], out[1]
-    assert mx0 == mx1 == [15.0, 3.0]                       # max over ranks, seen by all ranks
-    assert v0 == pytest.approx(16 * 2 * 7 / 0.015)         # 16 queries per rank, 2 ranks, 7 steps
-    assert s0 != s1                                        # independent batches per rank
+    (ms0, mx0, rate0, T0, steps, d0), (ms1, mx1, rate1, T1, _, d1) = out[0], out[1]
+    # every rank sees the slowest rank's measured time
+    assert mx0 == mx1 == pytest.approx(max(ms0, ms1))
+    # whole-job rate: all ranks' query tokens over the slowest rank's time
+    assert rate0 == rate1 == pytest.approx((T0 + T1) * steps / (max(ms0, ms1) / 1e3))
+    # independent batches per rank: different inputs, different attention outputs
+    assert d0 != d1
