@@ -246,6 +246,9 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  * accumulation in tensor memory).  A is bf16 [128, 64] row-major, B is bf16
  * [64, 64] row-major, D fp32 [128, 64].  `a_mn_major` / `b_mn_major` stage the
  * operand transposed (as the attention value and probability operands are).
+ * `swizzle_bytes` is 128 (128-byte swizzled atoms of 64 K-elements) or 64
+ * (64-byte swizzled atoms of 32 K-elements, K-major operands only, the way the
+ * attention stages its rope halves).
  *
  * dsa_selftest_topk_max_cluster: caps the thread-block cluster the top-k
  * launches use on the current device at `max_cluster` blocks (1, 2, 4, 8 or
@@ -258,7 +261,7 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  * as DSA_ERR_TIMEOUT.  Nothing faults; the context stays usable.
  */
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
-                              cudaStream_t stream);
+                              int32_t swizzle_bytes, cudaStream_t stream);
 dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster);
 dsa_status_t dsa_selftest_timeout(int32_t limit_ms, cudaStream_t stream);
 

@@ -93,7 +93,7 @@ def load() -> ctypes.CDLL:
     lib.dsa_sparse_mla_fwd_noalloc.argtypes = [POINTER(Batch), POINTER(MlaLayer), c_void_p, c_int64, c_int32,
                                                c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_mma.restype = c_int32
-    lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p]
+    lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]
     lib.dsa_selftest_topk_max_cluster.restype = c_int32
     lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
     lib.dsa_selftest_timeout.restype = c_int32
@@ -227,9 +227,9 @@ def check_device_error(stream=None) -> int:
 
 
 def selftest_mma(a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, a_mn_major: bool, b_mn_major: bool,
-                 stream=None):
-    _check(load().dsa_selftest_mma(_ptr(a), _ptr(b), _ptr(d), int(a_mn_major), int(b_mn_major), _stream(stream)),
-           "dsa_selftest_mma")
+                 swizzle_bytes: int = 128, stream=None):
+    _check(load().dsa_selftest_mma(_ptr(a), _ptr(b), _ptr(d), int(a_mn_major), int(b_mn_major), swizzle_bytes,
+                                   _stream(stream)), "dsa_selftest_mma")
 
 
 def selftest_topk_max_cluster(max_cluster: int):

@@ -264,9 +264,11 @@ CUresult encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank,
 // ------------------------------------------------------------- self-tests ---
 namespace {
 
-// One 128 x 64 x 64 tile through the same descriptors the kernels build.
+// One 128 x 64 tile through the same descriptors the kernels build.  With
+// sw64 the operands are K-major in 64-byte-swizzled atoms, two K-blocks of 32.
 __global__ void __launch_bounds__(128, 1)
-    selftest_mma_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int a_mn, int b_mn, int* err) {
+    selftest_mma_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int a_mn, int b_mn, int sw64,
+                        int* err) {
   __shared__ __align__(1024) uint8_t sa[128 * 128];  // 16 KB
   __shared__ __align__(1024) uint8_t sb[64 * 128];   // 8 KB
   __shared__ __align__(8) uint64_t bar;
@@ -277,9 +279,12 @@ __global__ void __launch_bounds__(128, 1)
   for (int i = tid; i < 128 * 64; i += 128) {
     const int m = i / 64, k = i % 64;
     uint32_t off;
-    if (!a_mn) {  // K-major: row m, 64 k per row
+    if (sw64) {          // K-block k/32 of [128 rows x 64 bytes]
+      const int kb = k / 32, kk = k % 32;
+      off = kb * 8192 + m * 64 + (((kk / 8) ^ ((m >> 1) & 3)) << 4) + (kk % 8) * 2;
+    } else if (!a_mn) {  // K-major: row m, 64 k per row
       off = m * 128 + (((k / 8) ^ (m & 7)) << 4) + (k % 8) * 2;
-    } else {      // MN-major: two 64-wide m blocks of 64 k-rows, 8 KB apart
+    } else {             // MN-major: two 64-wide m blocks of 64 k-rows, 8 KB apart
       const int mb = m / 64, mm = m % 64;
       off = mb * 8192 + k * 128 + (((mm / 8) ^ (k & 7)) << 4) + (mm % 8) * 2;
     }
@@ -288,8 +293,14 @@ __global__ void __launch_bounds__(128, 1)
   for (int i = tid; i < 64 * 64; i += 128) {
     const int n = i / 64, k = i % 64;
     uint32_t off;
-    if (!b_mn) off = n * 128 + (((k / 8) ^ (n & 7)) << 4) + (k % 8) * 2;
-    else off = k * 128 + (((n / 8) ^ (k & 7)) << 4) + (n % 8) * 2;
+    if (sw64) {
+      const int kb = k / 32, kk = k % 32;
+      off = kb * 4096 + n * 64 + (((kk / 8) ^ ((n >> 1) & 3)) << 4) + (kk % 8) * 2;
+    } else if (!b_mn) {
+      off = n * 128 + (((k / 8) ^ (n & 7)) << 4) + (k % 8) * 2;
+    } else {
+      off = k * 128 + (((n / 8) ^ (k & 7)) << 4) + (n % 8) * 2;
+    }
     *reinterpret_cast<__nv_bfloat16*>(sb + off) = B[i];
   }
   if (tid == 0) {
@@ -309,10 +320,16 @@ __global__ void __launch_bounds__(128, 1)
   if (tid == 0) {
     const uint32_t idesc = mma_idesc_bf16(128, 64, a_mn != 0, b_mn != 0);
     for (int ks = 0; ks < 4; ++ks) {
-      const uint64_t ad = a_mn ? smem_desc_sw128(smem_u32(sa) + ks * 2048, 8192, 1024)
-                               : smem_desc_sw128(smem_u32(sa) + ks * 32, 16, 1024);
-      const uint64_t bd = b_mn ? smem_desc_sw128(smem_u32(sb) + ks * 2048, 8192, 1024)
-                               : smem_desc_sw128(smem_u32(sb) + ks * 32, 16, 1024);
+      uint64_t ad, bd;
+      if (sw64) {
+        ad = smem_desc_sw64(smem_u32(sa) + (ks / 2) * 8192 + (ks % 2) * 32, 512);
+        bd = smem_desc_sw64(smem_u32(sb) + (ks / 2) * 4096 + (ks % 2) * 32, 512);
+      } else {
+        ad = a_mn ? smem_desc_sw128(smem_u32(sa) + ks * 2048, 8192, 1024)
+                  : smem_desc_sw128(smem_u32(sa) + ks * 32, 16, 1024);
+        bd = b_mn ? smem_desc_sw128(smem_u32(sb) + ks * 2048, 8192, 1024)
+                  : smem_desc_sw128(smem_u32(sb) + ks * 32, 16, 1024);
+      }
       mma_bf16(tmem, ad, bd, idesc, ks != 0);
     }
     mma_commit(smem_u32(&bar));
@@ -550,13 +567,15 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
 }
 
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
-                              cudaStream_t stream) {
+                              int32_t swizzle_bytes, cudaStream_t stream) {
   if (a == nullptr || b == nullptr || d == nullptr) return DSA_ERR_INVALID_ARG;
+  if (swizzle_bytes != 128 && swizzle_bytes != 64) return DSA_ERR_INVALID_ARG;
+  if (swizzle_bytes == 64 && (a_mn_major || b_mn_major)) return DSA_ERR_UNSUPPORTED;
   DeviceInfo dev;
   if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
   selftest_mma_kernel<<<1, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(a),
                                               static_cast<const __nv_bfloat16*>(b), d, a_mn_major, b_mn_major,
-                                              dev.err);
+                                              swizzle_bytes == 64, dev.err);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -22,16 +22,17 @@ def lib():
 
 # ------------------------------------------------ device machinery checks ---
 
-@pytest.mark.parametrize("a_mn,b_mn", [(False, False), (True, True), (True, False), (False, True)])
-def test_selftest_mma_tile(lib, a_mn, b_mn):
+@pytest.mark.parametrize("a_mn,b_mn,sw", [(False, False, 128), (True, True, 128), (True, False, 128),
+                                          (False, True, 128), (False, False, 64)])
+def test_selftest_mma_tile(lib, a_mn, b_mn, sw):
     g = torch.Generator().manual_seed(7)
     a = torch.randint(-4, 5, (128, 64), generator=g).to(torch.bfloat16).cuda()
     b = torch.randint(-4, 5, (64, 64), generator=g).to(torch.bfloat16).cuda()
     d = torch.zeros((128, 64), dtype=torch.float32, device="cuda")
-    lib.selftest_mma(a, b, d, a_mn, b_mn)
+    lib.selftest_mma(a, b, d, a_mn, b_mn, sw)
     assert lib.check_device_error() == lib.DSA_OK
     ref = a.double().cpu() @ b.double().cpu().T
-    assert torch.equal(d.cpu().double(), ref), f"tile mismatch (a_mn={a_mn}, b_mn={b_mn})"
+    assert torch.equal(d.cpu().double(), ref), f"tile mismatch (a_mn={a_mn}, b_mn={b_mn}, swizzle {sw})"
 
 
 def test_bounded_wait_reports_timeout(lib):
