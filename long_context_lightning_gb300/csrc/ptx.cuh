@@ -419,6 +419,21 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
+// Asynchronous store into another block of the cluster: the bytes are counted
+// on that block's mbarrier `bar_cluster` (complete_tx, release at cluster
+// scope), so the receiver needs no other signal and the sender no fence.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar_cluster)
+               : "memory");
+}
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

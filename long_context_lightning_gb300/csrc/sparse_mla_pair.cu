@@ -66,6 +66,9 @@ constexpr int kThreads = 416;
 constexpr int kMaxPairs = 8;
 constexpr int kPrefetchTiles = 6;      // tiles of rows prefetched into L2 ahead of their gather
 constexpr int kSlabHeader = 512;       // (m, l) x 64 heads, fp32
+constexpr int kXBytes = kRows * 32 * 4;       // the peer's partial of this block's heads
+constexpr int kPBytes = kRows * 64 + 33 * 4;  // the peer's P^T half, its flag and factors
+constexpr int kMLBytes = 64 * 4;              // the peer's (m, l) of its heads
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int OFF_QV = 0;                               // 4 x [64 heads x 64 dims], 128-byte swizzle
@@ -104,13 +107,13 @@ enum {
   B_SFULL = 10,     // [2] S^T partial formed (commit)
   B_SFREE = 12,     // [2] S^T buffer read by the softmax warps (8 arrivals)
   B_VALID = 14,     // [2] valid flags of the stage written (32 arrivals)
-  B_XFULL = 16,     // the peer's partial of this block's heads landed (8 remote arrivals)
+  B_XFULL = 16,     // the peer's partial of this block's heads landed (armed arrival + st.async bytes)
   B_XFREE = 17,     // the peer has read its partial from us (8 remote arrivals)
-  B_PFULL = 18,     // both P^T halves and messages written (8 local + 8 remote arrivals)
+  B_PFULL = 18,     // both P^T halves and the peer's message written (8 local arrivals + st.async bytes)
   B_PVDONE = 19,    // both blocks' PV of the tile completed (2 multicast commits)
   B_RESC = 20,      // O^T columns rescaled (8 arrivals)
   B_Q = 21,         // query landed
-  B_ML = 22,        // the peer's (m, l) landed
+  B_ML = 22,        // the peer's (m, l) landed (armed arrival + st.async bytes)
   B_READY = 23,     // same-half blocks of other pairs past their loops (remote arrivals)
   B_RECV = 24,      // slabs of the other pairs landed (bytes)
   B_DRAIN = 25,     // every issued MMA completed
@@ -246,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_SFREE + s), 8);
       mbar_init(bar(B_VALID + s), 32);
     }
-    mbar_init(bar(B_XFULL), 8);
+    mbar_init(bar(B_XFULL), 1);
     mbar_init(bar(B_XFREE), 8);
-    mbar_init(bar(B_PFULL), 16);
+    mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_PVDONE), 2);
     mbar_init(bar(B_RESC), 8);
     mbar_init(bar(B_Q), 1);
@@ -262,6 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     lo->lse = L.lse;
     lo->H = L.H;
     fence_mbar_init();
+    // the peer's first partial and its (m, l) are counted in bytes; these
+    // arrivals open the phases (later partials are armed as each one is read)
+    mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
+    mbar_arrive_expect_tx(bar(B_ML), kMLBytes);
     prefetch_tmap(tm_cv);
     prefetch_tmap(tm_cr);
     // the other pairs' slabs are counted in bytes; this arrival opens the phase
@@ -416,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (npv < my_tiles && !bad) {
         bool did = false;
         if (npv < ns && mbar_test_wait_cluster(bar(B_PFULL), (uint32_t)npv & 1u)) {
-          fence_proxy_async_smem();  // P^T halves were written by threads of both blocks
+          fence_proxy_async_smem();  // the peer's P^T half came by st.async
           tc_fence_after();
           const int* msg = reinterpret_cast<const int*>(msg_s + (npv & 1) * 2 * MSG_WORDS);
           if ((msg[0] | msg[MSG_WORDS]) != 0) {  // a reference moved: O^T is rescaled first
@@ -522,16 +529,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       if (jj >= 1) bad |= !mbar_wait_cl(bar(B_XFREE), (uint32_t)(jj - 1) & 1u, abort_flag, p.err);
       if (!bad) {
+        const uint32_t xbar = dsmem_addr(bar(B_XFULL), peer);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const uint32_t a = srecv_row + ((uint32_t)((4 * g + i) ^ (srow & 7)) << 4);
-          st_dsmem_v4(dsmem_addr(a, peer), r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+          st_async_v4(dsmem_addr(a, peer), r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3], xbar);
         }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        fence_acq_rel_cluster();
-        mbar_arrive_remote(dsmem_addr(bar(B_XFULL), peer));
       }
       // this block's heads: own partial plus the peer's partial
       tmem_ld16(scol + own0, r);
@@ -549,7 +552,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        fence_acq_rel_cluster();
+        // every warp has passed this phase before the peer may send the next
+        // partial, so the next phase can be armed now
+        if (warp == 5 && jj + 1 < my_tiles) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
         mbar_arrive_remote(dsmem_addr(bar(B_XFREE), peer));  // the peer may send its next partial
         mbar_arrive(bar(B_SFREE + bs));                      // S^T buffer free for the tile after next
       }
@@ -601,28 +606,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (jj >= 1) bad |= !mbar_wait_cl(bar(B_PVDONE), (uint32_t)(jj - 1) & 1u, abort_flag, p.err);
       float* msg_own = msg_s + bs * 2 * MSG_WORDS;
       const uint32_t msg_peer = dsmem_addr(smem_u32(msg_own + MSG_WORDS), peer);
+      const uint32_t pbar = dsmem_addr(bar(B_PFULL), peer);
       if (st < 32) {
         const float a = moved ? alpha_s[st] : 1.f;
         msg_own[4 + st] = a;
-        if (!bad) st_dsmem_f32(msg_peer + (uint32_t)(4 + st) * 4u, a);
+        if (!bad) st_async_b32(msg_peer + (uint32_t)(4 + st) * 4u, __float_as_uint(a), pbar);
       }
       if (st == 0) {
         reinterpret_cast<int*>(msg_own)[0] = moved ? 1 : 0;
-        if (!bad) st_dsmem_u32(msg_peer, moved ? 1u : 0u);
+        if (!bad) st_async_b32(msg_peer, moved ? 1u : 0u, pbar);
       }
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t a = pt_row + ((uint32_t)((4 * half + 2 * g + cc) ^ (srow & 7)) << 4);
         st_shared_v4(a, w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
-        if (!bad) st_dsmem_v4(dsmem_addr(a, peer), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+        if (!bad) st_async_v4(dsmem_addr(a, peer), w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3], pbar);
       }
-      fence_proxy_async_smem();
-      fence_proxy_async_cluster();
+      fence_proxy_async_smem();  // this block's tensor core reads the P^T written here
       __syncwarp();
       if (lane == 0) {
-        fence_acq_rel_cluster();
-        mbar_arrive_cl(bar(B_PFULL));
-        mbar_arrive_remote(dsmem_addr(bar(B_PFULL), peer));
+        // the peer's half and message arrive as bytes on this phase
+        if (warp == 5) mbar_arrive_expect_tx(bar(B_PFULL), kPBytes);
+        else mbar_arrive(bar(B_PFULL));
       }
       // a reference moved in either block: rescale this block's O^T columns of
       // the moved heads before the PV (the previous PV has completed)
@@ -664,13 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m = mref_s[st];
       ml_s[h] = m;
       ml_s[64 + h] = l;
-      st_dsmem_f32(dsmem_addr(smem_u32(ml_s + h), peer), m);
-      st_dsmem_f32(dsmem_addr(smem_u32(ml_s + 64 + h), peer), l);
-      __syncwarp();
-      if (st == 0) {
-        fence_acq_rel_cluster();
-        mbar_arrive_remote(dsmem_addr(bar(B_ML), peer));
-      }
+      const uint32_t mlbar = dsmem_addr(bar(B_ML), peer);
+      st_async_b32(dsmem_addr(smem_u32(ml_s + h), peer), __float_as_uint(m), mlbar);
+      st_async_b32(dsmem_addr(smem_u32(ml_s + 64 + h), peer), __float_as_uint(l), mlbar);
     }
     bad |= !mbar_wait_cl(bar(B_ML), 0, abort_flag, p.err);
     if (my_tiles > 0) bad |= !mbar_wait_cl(bar(B_PVDONE), (uint32_t)(my_tiles - 1) & 1u, abort_flag, p.err);
