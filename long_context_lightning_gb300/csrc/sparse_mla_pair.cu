@@ -30,12 +30,14 @@
 // it); the owner sends the move's factors with its P^T half, and each block
 // rescales its own O^T columns of the moved heads before the PV.
 //
-// Row gather.  Rows land by TMA tile::gather4 (four rows per instruction):
-// the four value blocks as [128 rows x 64 dims] 128-byte-swizzled blocks, the
-// rope half as [128 rows x 32 dims] 64-byte-swizzled.  A stage is released in
-// parts: the rope half once its S^T run is done, value blocks 0-1 and 2-3 as
-// the two PV runs that read them complete.  Rows of later tiles are
-// bulk-prefetched into L2 a few tiles ahead, half of them by each block.
+// Row gather.  Rows land by 16-byte cp.async (a warp instruction moves four
+// 128-byte row pieces; tile::gather4 issues at about 31 ns per instruction per
+// warp, too slow for a 72 KB stage per tile): the four value blocks as [128
+// rows x 64 dims] 128-byte-swizzled blocks, the rope half as [128 rows x 32
+// dims] 64-byte-swizzled.  A stage is released in two parts as the two PV runs
+// that read it complete (value blocks 0-1; value blocks 2-3 and the rope
+// half).  Rows of later tiles are bulk-prefetched into L2 a few tiles ahead,
+// half of them by each block, so the copies read L2.
 //
 // Split over pairs: the selected rows of a query are divided among the pairs
 // of a cluster (1, 2, 4 or 8 pairs); the blocks that hold the same value half
@@ -43,8 +45,9 @@
 // shared memory.
 //
 // Warp roles (416 threads, one block per SM):
-//   warps 0..3   row gather: warp w owns value block w of each tile, warp 0
-//                also the rope half and the tile's valid flags; L2 prefetch
+//   warps 0..3   row gather: warp w owns value block w of each tile, warps 2
+//                and 3 also half the rope half each, warp 0 the tile's valid
+//                flags; L2 prefetch
 //   warp 4       TMEM owner, query TMA, MMA issuer (one thread)
 //   warps 5..12  S^T exchange, softmax of this block's 32 heads (one key and
 //                16 heads per thread), P^T, O^T rescale; then the output
@@ -99,16 +102,14 @@ constexpr int S_COL = 128;
 
 // barrier indices
 enum {
-  B_FA = 0,         // [2] stage parts a (rope half, value blocks 0-1) landed: 3 arrivals + bytes
-  B_FB = 2,         // [2] stage part b (value blocks 2-3) landed: 2 arrivals + bytes
-  B_RFREE = 4,      // [2] rope half read by S^T (commit)
+  B_FA = 0,         // [2] stage part a (value blocks 0-1) landed: 2 warp arrivals
+  B_FB = 2,         // [2] stage part b (value blocks 2-3, rope half) landed: 2 warp arrivals
   B_V01FREE = 6,    // [2] value blocks 0-1 read by the PV (commit)
-  B_V23FREE = 8,    // [2] value blocks 2-3 read by the PV (commit)
+  B_V23FREE = 8,    // [2] value blocks 2-3 read by the PV, rope half by S^T (commit)
   B_SFULL = 10,     // [2] S^T partial formed (commit)
   B_SFREE = 12,     // [2] S^T buffer read by the softmax warps (8 arrivals)
   B_VALID = 14,     // [2] valid flags of the stage written (32 arrivals)
   B_XFULL = 16,     // the peer's partial of this block's heads landed (armed arrival + st.async bytes)
-  B_XFREE = 17,     // the peer has read its partial from us (8 remote arrivals)
   B_PFULL = 18,     // both P^T halves and the peer's message written (8 local arrivals + st.async bytes)
   B_PVDONE = 19,    // both blocks' PV of the tile completed (2 multicast commits)
   B_RESC = 20,      // O^T columns rescaled (8 arrivals)
@@ -129,8 +130,6 @@ struct LayerOut {
 struct PairMaps {
   CUtensorMap qv[DSA_MAX_LAYERS];  // query value dims: box {64 dims, 64 heads, 1 query}, 128-byte swizzle
   CUtensorMap qr[DSA_MAX_LAYERS];  // query rope dims: box {32, 64, 1}, 64-byte swizzle
-  CUtensorMap cv[DSA_MAX_LAYERS];  // latent pool for gather4: box {64 dims, 1 row}, 128-byte swizzle
-  CUtensorMap cr[DSA_MAX_LAYERS];  // latent pool for gather4: box {32 dims, 1 row}, 64-byte swizzle
 };
 
 struct PairParams {
@@ -231,8 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const MlaLayerView& L = p.layer[li];
   const CUtensorMap* tm_qv = &maps.qv[li];
   const CUtensorMap* tm_qr = &maps.qr[li];
-  const CUtensorMap* tm_cv = &maps.cv[li];
-  const CUtensorMap* tm_cr = &maps.cr[li];
   // combine: the blocks of one value half split its 256 dims, `slice` each
   const int slice = 256 / npairs;
   const int ls = __ffs(slice) - 1;
@@ -240,9 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(B_FA + s), 3);
+      mbar_init(bar(B_FA + s), 2);
       mbar_init(bar(B_FB + s), 2);
-      mbar_init(bar(B_RFREE + s), 1);
       mbar_init(bar(B_V01FREE + s), 1);
       mbar_init(bar(B_V23FREE + s), 1);
       mbar_init(bar(B_SFULL + s), 1);
@@ -250,7 +246,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(B_VALID + s), 32);
     }
     mbar_init(bar(B_XFULL), 1);
-    mbar_init(bar(B_XFREE), 8);
     mbar_init(bar(B_PFULL), 8);
     mbar_init(bar(B_PVDONE), 2);
     mbar_init(bar(B_RESC), 8);
@@ -269,8 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // arrivals open the phases (later partials are armed as each one is read)
     mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
     mbar_arrive_expect_tx(bar(B_ML), kMLBytes);
-    prefetch_tmap(tm_cv);
-    prefetch_tmap(tm_cr);
     // the other pairs' slabs are counted in bytes; this arrival opens the phase
     if (npairs > 1) mbar_arrive_expect_tx(bar(B_RECV), (uint32_t)(npairs - 1) * slab_bytes);
   }
@@ -313,14 +306,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------ row gather
-    // Lane l of a gathering warp resolves rows 4l..4l+3 of a tile to pool rows.
+    // Lane l of a gathering warp resolves rows l, l+32, l+64, l+96 of a tile
+    // to pool rows (r4[k] = row 32k + l).
     const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
     int32_t r4[4];
     bool v4[4];
     auto resolve = [&](int jj) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int e = (j0 + jj) * kRows + 4 * lane + k;
+        const int e = (j0 + jj) * kRows + 32 * k + lane;
         int pos = e < nvalid ? __ldg(idx_row + e) : -1;
         if (pos >= n_t || pos < -1) {
           if (warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
@@ -340,38 +334,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         r4[k] = row >= 0 ? (int32_t)row : 0;  // an unused slot reads pool row 0 (finite data; weight 0)
       }
     };
+    const char* pool = reinterpret_cast<const char*>(L.kv.base);
+    const int64_t pitch = L.kv.row_stride * 2;  // bytes between pool rows
     bool bad = false;
-    int last_tile[2] = {-1, -1};
     auto issue = [&](int jj) {
       const int s = jj & 1;
       const uint32_t par = ((uint32_t)(jj >> 1) & 1u) ^ 1u;  // phase of this stage's previous use
       const uint32_t st_base = sbase + OFF_ST + s * STAGE;
-      if (warp == 0) {
-        // rope half: free once the previous tile of this stage has formed S^T
-        if (jj >= 2) bad |= !mbar_wait(bar(B_RFREE + s), par, abort_flag, p.err);
-        if (lane == 0) mbar_arrive_expect_tx(bar(B_FA + s), kRBlk);
-        __syncwarp();
-        if (!bad)
-          tma_gather4(st_base + 4 * kVBlk + lane * 256, tm_cr, bar(B_FA + s), 512 + 32 * half, r4[0], r4[1], r4[2],
-                      r4[3]);
-      }
       const int kb = warp;
-      const uint32_t fbar = bar((kb < 2 ? B_FA : B_FB) + s);
       if (jj >= 2) bad |= !mbar_wait(bar((kb < 2 ? B_V01FREE : B_V23FREE) + s), par, abort_flag, p.err);
       if (warp == 0) {
         // the previous tile of this stage has finished its PV: its softmax read these
 #pragma unroll
-        for (int k = 0; k < 4; ++k) valid_s[s * kRows + 4 * lane + k] = v4[k];
+        for (int k = 0; k < 4; ++k) valid_s[s * kRows + 32 * k + lane] = v4[k];
         mbar_arrive(bar(B_VALID + s));
       }
-      if (lane == 0) mbar_arrive_expect_tx(fbar, kVBlk);
+      if (!bad) {
+        // value block kb: instruction i moves rows 4i..4i+3, eight lanes (16-byte
+        // chunks c) per row
+        const int c = lane & 7;
+        const char* src0 = pool + (256 * half + 64 * kb) * 2 + c * 16;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int row = 4 * i + (lane >> 3);
+          const int32_t pr = __shfl_sync(0xffffffffu, r4[i >> 3], row & 31);  // i >> 3 is a constant here
+          cp_async_16(st_base + kb * kVBlk + row * 128 + ((c ^ (row & 7)) << 4), src0 + (int64_t)pr * pitch, 16);
+        }
+        if (warp >= 2) {
+          // rope half, rows 64 (w - 2) .. +63: instruction i moves eight rows, four
+          // lanes (16-byte chunks c) per row
+          const int cr = lane & 3;
+          const char* srcr = pool + (512 + 32 * half) * 2 + cr * 16;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int row = 64 * (warp - 2) + 8 * i + (lane >> 2);
+            const int32_t src_k = warp == 2 ? (i < 4 ? r4[0] : r4[1]) : (i < 4 ? r4[2] : r4[3]);  // r4[row >> 5]
+            const int32_t pr = __shfl_sync(0xffffffffu, src_k, row & 31);
+            cp_async_16(st_base + 4 * kVBlk + row * 64 + ((cr ^ ((row >> 1) & 3)) << 4), srcr + (int64_t)pr * pitch,
+                        16);
+          }
+        }
+      }
+      cp_async_commit();
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // the tensor cores read what cp.async wrote
       __syncwarp();
-      if (!bad)
-        tma_gather4(st_base + kb * kVBlk + lane * 512, tm_cv, fbar, 256 * half + 64 * kb, r4[0], r4[1], r4[2], r4[3]);
-      last_tile[s] = jj;
+      if (lane == 0) mbar_arrive(bar((kb < 2 ? B_FA : B_FB) + s));
     };
-    // rows of a later tile into L2: row 4l + w of the tile for the lanes of this
-    // block's parity, so that the pair prefetches each row once
+    // rows of a later tile into L2: row 32k + l of the tile for k = warp, the
+    // lanes of this block's parity, so that the pair prefetches each row once
     auto prefetch = [&](int jj) {
       resolve(jj);
       int32_t rp = r4[0];
@@ -394,14 +405,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       resolve(jj);
       issue(jj);
       if (jj + kPrefetchTiles < my_tiles) prefetch(jj + kPrefetchTiles);
-    }
-    if (*abort_flag) {
-      // copies already issued land before the block may go away
-      for (int s = 0; s < 2; ++s)
-        if (last_tile[s] >= 0) {
-          const uint32_t ph = (uint32_t)(last_tile[s] >> 1) & 1u;
-          mbar_wait_drain(bar((warp < 2 ? B_FA : B_FB) + s), ph);
-        }
     }
   } else if (warp == 4) {
     // ---------------------------------------------- query TMA + MMA issuer
@@ -457,17 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (mbar_test_wait(bar(B_FA + s), ph) &&
                 (ns < 2 || mbar_test_wait(bar(B_SFREE + (ns & 1)), ph ^ 1u))) {
               tc_fence_after();
-              const uint64_t dr = smem_desc_sw64(vb + 4 * kVBlk, 512);
-#pragma unroll
-              for (int kk = 0; kk < 2; ++kk)
-                mma_bf16(scol, dr + (uint64_t)((kk * 32) >> 4), dqr + (uint64_t)((kk * 32) >> 4), idesc_s, kk != 0);
 #pragma unroll
               for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                   mma_bf16(scol, dk + (uint64_t)((kb * kVBlk + kk * 32) >> 4),
-                           dqv + (uint64_t)((kb * kQBlk + kk * 32) >> 4), idesc_s, 1u);
-              mma_commit(bar(B_RFREE + s));
+                           dqv + (uint64_t)((kb * kQBlk + kk * 32) >> 4), idesc_s, (kb | kk) != 0);
               part = 1;
               did = true;
             }
@@ -479,6 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int kk = 0; kk < 4; ++kk)
                 mma_bf16(scol, dk + (uint64_t)((kb * kVBlk + kk * 32) >> 4),
                          dqv + (uint64_t)((kb * kQBlk + kk * 32) >> 4), idesc_s, 1u);
+            const uint64_t dr = smem_desc_sw64(vb + 4 * kVBlk, 512);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+              mma_bf16(scol, dr + (uint64_t)((kk * 32) >> 4), dqr + (uint64_t)((kk * 32) >> 4), idesc_s, 1u);
             mma_commit(bar(B_SFULL + (ns & 1)));
             part = 0;
             ++ns;
@@ -524,10 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t scol = lane_base + S_COL + 64 * bs;
       uint32_t r[16];
-      // the peer's heads of this block's partial go to the peer
+      // the peer's heads of this block's partial go to the peer.  Its buffer is
+      // free: the peer read the previous partial before it sent its P^T half of
+      // the previous tile, which this thread waited for (st.async completes
+      // with release semantics)
       tmem_ld16(scol + oth0, r);
       tmem_wait_ld();
-      if (jj >= 1) bad |= !mbar_wait_cl(bar(B_XFREE), (uint32_t)(jj - 1) & 1u, abort_flag, p.err);
       if (!bad) {
         const uint32_t xbar = dsmem_addr(bar(B_XFULL), peer);
 #pragma unroll
@@ -553,10 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         // every warp has passed this phase before the peer may send the next
-        // partial, so the next phase can be armed now
+        // partial (it waits for this tile's P^T half first), so the next phase
+        // can be armed now
         if (warp == 5 && jj + 1 < my_tiles) mbar_arrive_expect_tx(bar(B_XFULL), kXBytes);
-        mbar_arrive_remote(dsmem_addr(bar(B_XFREE), peer));  // the peer may send its next partial
-        mbar_arrive(bar(B_SFREE + bs));                      // S^T buffer free for the tile after next
+        mbar_arrive(bar(B_SFREE + bs));  // S^T buffer free for the tile after next
       }
       bad |= !mbar_wait(bar(B_VALID + bs), ph, abort_flag, p.err);
       const bool kv = valid_s[bs * kRows + srow] != 0;
@@ -850,17 +854,6 @@ cudaError_t launch_sparse_mla_pair(const MlaLaunch& a, cudaStream_t stream) {
       if (encode_tmap(&maps.qv[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, lv.q, dims, strides, box_v,
                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
           encode_tmap(&maps.qr[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, lv.q, dims, strides, box_r,
-                      CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    }
-    {  // latent pool rows for tile::gather4: boxes one row high
-      const uint64_t dims[2] = {576u, (uint64_t)lv.kv.num_rows};
-      const uint64_t strides[1] = {(uint64_t)lv.kv.row_stride * 2};
-      const uint32_t box_v[2] = {64u, 1u};
-      const uint32_t box_r[2] = {32u, 1u};
-      if (encode_tmap(&maps.cv[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lv.kv.base, dims, strides, box_v,
-                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-          encode_tmap(&maps.cr[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lv.kv.base, dims, strides, box_r,
                       CU_TENSOR_MAP_SWIZZLE_64B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
