@@ -153,8 +153,6 @@ struct MlaLaunch {
   bool plan_early = false;  // as in TopkLaunch
 };
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
-// The 576-dim latent (512 value + 64 rope dims): columns split over block pairs.
-cudaError_t launch_sparse_mla_pair(const MlaLaunch& a, cudaStream_t stream);
 
 // Largest thread-block cluster (8, or 16 where the device schedules it) for
 // kernel `kern` launched with `threads` threads and `smem` bytes of dynamic

@@ -744,9 +744,8 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
 
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  // the 576-dim latent runs on block pairs that split its columns
-  if (a.d_qk == 576 && a.d_v == 512) return launch_sparse_mla_pair(a, stream);
   // P^T lives in the last column block of a stage: the value dims end before it
+  if (a.d_qk == 576 && a.d_v == 512) return launch_t<9, 4>(a, stream, 0);
   if (a.d_qk == 80 && a.d_v == 64) return launch_t<2, 1>(a, stream, 1);
   return cudaErrorInvalidValue;
 }
