@@ -9,15 +9,15 @@
 //
 // Row gather.  The selected rows of a query are taken 128 at a time into one
 // tile of shared memory, D/64 column blocks of [128 rows x 64 dims] (128-byte
-// swizzle), by 16-byte cp.async (one warp instruction moves four 128-byte row
-// pieces).  Softmax warp j refills column block j as soon as the PV MMAs that
-// read it complete (the softmax warps are idle while the PV runs), so the
-// next tile's copies overlap the end of this tile's PV; the gather warps refill
-// the last block (it holds P^T during the PV, so it is freed last).  Every row
-// of the block's later tiles is bulk-prefetched into L2 at the start, so HBM
-// streams at full rate while the tiles are consumed and the copies read L2.
-// (TMA tile::gather4 issues at ~31 ns per instruction per warp: 2 x 32 per
-// tile per warp left each tile's refill issue-bound for over 2 us.)
+// swizzle), by TMA tile::gather4 (four rows x 64 dims per instruction).  A
+// gather4 costs its warp ~30 ns (lanes in series), so the copies are spread:
+// gather warp w owns the column blocks w and w+4, and the last block (it holds
+// P^T during the PV, so it is freed last) is gathered by the eight softmax
+// warps, idle at that point.  Each column block is refilled as soon as the PV
+// MMAs that read it complete, so the next tile's copies overlap the end of
+// this tile's PV; and once a tile has landed, the next tile's rows are
+// bulk-prefetched into L2 (HBM is otherwise idle while a tile is consumed), so
+// those copies read L2.
 //
 // Tensor cores.  The same tile serves two MMAs:
 //   S^T[key, h] = C[key, :] . Q[h, :]^T     M = 128 keys, N = 64 heads, K = D
@@ -46,14 +46,12 @@
 // traffic.
 //
 // Warp roles (416 threads, one block per SM):
-//   warps 0..3   the last column block's copies (index -> pool row, paged or
-//                contiguous); L2 prefetch of the block's later tiles
+//   warps 0..3   row gather (index -> pool row, paged or contiguous) of the
+//                column blocks before the last; next tile's L2 prefetch
 //   warp 4       TMEM owner, query TMA, MMA issuer (one thread)
 //   warps 5..12  softmax: two warps per TMEM lane quadrant, 32 heads each;
-//                softmax warp j copies column block j of every tile; then the
-//                combine
+//                the last column block's gather; then the combine
 #include <algorithm>
-#include <type_traits>
 
 #include "internal.cuh"
 
@@ -76,7 +74,8 @@ struct MlaCfg {
   static constexpr int STAGE = NB * kBlk;                 // one tile of gathered rows
   static constexpr int OFF_Q = 0;                         // NB x [64 heads x 64 dims]
   static constexpr int OFF_KV = OFF_Q + NB * 64 * 128;    // NB blocks of [128 rows x 64 dims]
-  static constexpr int OFF_RED = OFF_KV + STAGE;            // 4 x 64 float
+  static constexpr int OFF_VALID = OFF_KV + STAGE;        // 128 int
+  static constexpr int OFF_RED = OFF_VALID + kRows * 4;      // 4 x 64 float
   static constexpr int OFF_MREF = OFF_RED + 4 * 64 * 4;      // 64 float
   static constexpr int OFF_ALPHA = OFF_MREF + 64 * 4;        // 64 float
   static constexpr int OFF_F = OFF_ALPHA + 64 * 4;           // kMaxSplit x 64 float
@@ -169,11 +168,14 @@ template <int NB, int MB>
 __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
                       const __grid_constant__ CUtensorMap tm_q2, const __grid_constant__ CUtensorMap tm_q3,
+                      const __grid_constant__ CUtensorMap tm_c0, const __grid_constant__ CUtensorMap tm_c1,
+                      const __grid_constant__ CUtensorMap tm_c2, const __grid_constant__ CUtensorMap tm_c3,
                       MlaParams p) {
   using C = MlaCfg<NB, MB>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
+  int* valid_s = reinterpret_cast<int*>(smem + C::OFF_VALID);
   float* red_s = reinterpret_cast<float*>(smem + C::OFF_RED);
   float* mref_s = reinterpret_cast<float*>(smem + C::OFF_MREF);
   float* alpha_s = reinterpret_cast<float*>(smem + C::OFF_ALPHA);
@@ -183,17 +185,15 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   // one phase per tile each: column blocks [0, NB_A) / [NB_A, NB) of the tile
-  // landed (one arrival per copying warp); column block kb read by every MMA
-  // of the tile (commit); S^T formed (commit); P^T written (softmax threads)
+  // landed (bytes); column block kb read by every MMA of the tile (commit);
+  // S^T formed (commit); P^T written (softmax threads); the tile's valid flags
+  // written (gather warp 0)
   constexpr int NB_A = (NB + 1) / 2;  // blocks of the first S^T run
-  // copying warps of each part: softmax warp j copies block j < NB-1, the four
-  // gather warps block NB-1
-  constexpr int kFullA = NB_A < NB - 1 ? NB_A : NB - 1;
-  constexpr int kFullB = (NB - 1 - kFullA) + 4;
   auto bar_full = [&](int part) { return smem_u32(bars + part); };
   auto bar_empty = [&](int kb) { return smem_u32(bars + 2 + kb); };
   const uint32_t bar_s_full = smem_u32(bars + NB + 2);
   const uint32_t bar_p_full = smem_u32(bars + NB + 3);
+  const uint32_t bar_valid = smem_u32(bars + NB + 4);
   const uint32_t bar_q_full = smem_u32(bars + NB + 5);
   const uint32_t bar_o_done = smem_u32(bars + NB + 6);
   const uint32_t bar_drain = smem_u32(bars + NB + 7);
@@ -207,15 +207,17 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
   const int li = blockIdx.y / p.T;
   const MlaLayerView& L = p.layer[li];
   const CUtensorMap* tm_q = li == 0 ? &tm_q0 : li == 1 ? &tm_q1 : li == 2 ? &tm_q2 : &tm_q3;
+  const CUtensorMap* tm_c = li == 0 ? &tm_c0 : li == 1 ? &tm_c1 : li == 2 ? &tm_c2 : &tm_c3;
   const int slice = p.d_v / (int)csize;  // value dims owned by each block of the cluster
   // a slab: header, then [32 head pairs][slice value dims] words (bf16 pairs)
   const uint32_t slab_bytes = (uint32_t)(kSlabHeader + slice * 32 * 4);
   const int ls = __ffs(slice) - 1;  // slice is a power of two (d_v and the cluster size are)
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_full(0), kFullA);
-    mbar_init(bar_full(1), kFullB);
+    mbar_init(bar_full(0), 1);
+    mbar_init(bar_full(1), 1);
     for (int kb = 0; kb < NB; ++kb) mbar_init(bar_empty(kb), 1);
+    mbar_init(bar_valid, 32);
     mbar_init(bar_s_full, 1);
     mbar_init(bar_p_full, kSoftmaxThreads);
     mbar_init(bar_q_full, 1);
@@ -232,6 +234,7 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     lo->H = L.H;
     lo->d_v = p.d_v;
     fence_mbar_init();
+    prefetch_tmap(tm_c);
     // the peers' slabs are counted in bytes; this arrival opens the phase
     if (csize > 1) mbar_arrive_expect_tx(bar_recv, (csize - 1) * slab_bytes);
   }
@@ -274,21 +277,17 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     const int j0 = (int)((int64_t)tiles * crank / csize), j1 = (int)((int64_t)tiles * (crank + 1) / csize);
     my_tiles = j1 - j0;
 
-    // Lane l of a copying warp resolves rows l, l+32, l+64, l+96 of a tile to
-    // pool rows (r4[k] = row 32k + l); a softmax thread reads its own key's
-    // validity from the same table (key 32 quad + lane is r4[quad]).
+    // Lane l of a gathering warp resolves rows 4l..4l+3 of a tile to pool rows.
     const int32_t* idx_row = p.idx + (int64_t)t * p.ld_idx;
-    const char* pool = reinterpret_cast<const char*>(L.kv.base);
-    const int64_t pitch = L.kv.row_stride * 2;  // bytes between pool rows
     int32_t r4[4];
     bool v4[4];
     auto resolve = [&](int jj) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int e = (j0 + jj) * kRows + 32 * k + lane;
+        const int e = (j0 + jj) * kRows + 4 * lane + k;
         int pos = e < nvalid ? __ldg(idx_row + e) : -1;
         if (pos >= n_t || pos < -1) {
-          if (warp == 5) atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          if (warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
           pos = -1;
         }
         int64_t row = -1;
@@ -299,68 +298,66 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
             row = seq_base + pos;
             if (row < 0 || row >= L.kv.num_rows) row = -1;
           }
-          if (row < 0 && warp == 5) atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          if (row < 0 && warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
         }
         v4[k] = row >= 0;
         r4[k] = row >= 0 ? (int32_t)row : 0;  // an unused slot reads pool row 0 (finite data; weight 0)
       }
     };
-    // 16-byte copies of column block kb of the tile: instruction i moves rows
-    // row0 + 4i .. +3, eight lanes (chunks c) per row; chunks past d_qk are
-    // zero-filled without a read.  `rowsel(i)` gives the r4 entry holding the
-    // instruction's rows; lane (row & 31) holds each row.
-    auto copy_block = [&](int kb, int row0, auto n_instr, auto rowsel) {
-      const int c = lane & 7;
-      const int col = kb * 64 + c * 8;
-      const uint32_t nbytes = col < p.d_qk ? 16u : 0u;
-      const char* src0 = pool + (nbytes ? col * 2 : 0);
-#pragma unroll
-      for (int i = 0; i < decltype(n_instr)::value; ++i) {
-        const int row = row0 + 4 * i + (lane >> 3);
-        const int32_t pr = __shfl_sync(0xffffffffu, rowsel(i), row & 31);
-        cp_async_16(sbase + C::OFF_KV + kb * kBlk + row * 128 + ((c ^ (row & 7)) << 4), src0 + (int64_t)pr * pitch,
-                    nbytes);
-      }
-    };
-    // the tensor cores read what cp.async wrote: wait, make it visible to the
-    // async proxy, then one arrival per warp
-    auto land = [&](int part) {
-      cp_async_commit();
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_full(part));
+    // Column block NB-1 (it holds P^T while the PV runs, so it is released
+    // last) is gathered by the softmax warps, idle at that point: lanes
+    // 4j..4j+3 of softmax warp j, four copies per warp rather than one warp's
+    // thirty-two.
+    auto gather_last_block = [&]() {
+      if ((lane >> 2) == warp - 5)
+        tma_gather4(sbase + C::OFF_KV + lane * 512 + (NB - 1) * kBlk, tm_c, bar_full(1), (NB - 1) * 64, r4[0], r4[1], r4[2],
+                    r4[3]);
     };
 
     if (warp < 4) {
-      // ----------------------------------------------- last block + L2 prefetch
-      // Warp w copies rows 32w..32w+31 of column block NB-1 once the PV of the
-      // previous tile has completed.  Before its first wait it streams every
-      // row of the block's later tiles into L2 (one bulk prefetch per row;
-      // the index loads of a batch of tiles are in flight together).
+      // ------------------------------------------------------------ row gather
+      // Warp w owns the column blocks kb = w, w+4 < NB-1 of every tile and
+      // gathers its lanes' rows for each of them.  A block is refilled as soon
+      // as the PV that reads it has completed; S^T waits for the whole tile.
       bool bad = false;
-      auto my_rows = [&]() { return warp == 0 ? r4[0] : warp == 1 ? r4[1] : warp == 2 ? r4[2] : r4[3]; };
+      if (my_tiles > 0) resolve(0);
       for (int jj = 0; jj < my_tiles; ++jj) {
-        resolve(jj);
-        if (jj > 0) bad |= !mbar_wait(bar_empty(NB - 1), (jj - 1) & 1, abort_flag, p.err);
-        if (!bad) copy_block(NB - 1, 32 * warp, std::integral_constant<int, 8>(), [&](int) { return my_rows(); });
-        if (jj == 0) {
-          for (int j = 1; j < my_tiles; j += 4) {
-            int pos[4];
+        const uint32_t par = (jj & 1) ^ 1;  // phase of the previous tile
+        const uint32_t dst = sbase + C::OFF_KV + lane * 512;
+        for (int kb = warp; kb < NB - 1; kb += 4) {
+          bad |= !mbar_wait(bar_empty(kb), par, abort_flag, p.err);
+          if (kb == 0) {
+            // block 0 is released by the first MMA group of the previous PV,
+            // issued after that tile's softmax had read these flags
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int e = (j0 + j + u) * kRows + 32 * warp + lane;
-              pos[u] = (j + u < my_tiles && e < nvalid) ? __ldg(idx_row + e) : -1;
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              if (pos[u] < 0 || pos[u] >= n_t) continue;
-              const int64_t row = L.kv.paged ? cache_row(L.kv, b, pos[u]) : seq_base + pos[u];
-              if (row >= 0 && row < L.kv.num_rows) prefetch_l2_bulk(pool + row * pitch, (uint32_t)p.d_qk * 2u);
+            for (int k = 0; k < 4; ++k) valid_s[4 * lane + k] = v4[k];
+            mbar_arrive(bar_valid);
+            // one arrival with each part's bytes opens its phase; blocks of other
+            // warps may land before it (the count goes negative).  Block 0 is
+            // released after the previous S^T, so both previous phases are done.
+            if (lane == 0) {
+              mbar_arrive_expect_tx(bar_full(0), NB_A * kBlk);
+              mbar_arrive_expect_tx(bar_full(1), (NB - NB_A) * kBlk);
             }
           }
+          __syncwarp();
+          const uint32_t bar = bar_full(kb < NB_A ? 0 : 1);
+          if (!bad) tma_gather4(dst + kb * kBlk, tm_c, bar, kb * 64, r4[0], r4[1], r4[2], r4[3]);
         }
-        land(1);
+        if (jj + 1 < my_tiles) {
+          // Shared memory holds one tile.  Once this tile has landed, HBM is idle
+          // while it is consumed: the next tile's rows stream into L2 then, and
+          // its gathers read L2.  The four warps split the rows (lane l, warp w:
+          // row 4l + w), one bulk prefetch of a whole row each.
+          resolve(jj + 1);
+          int32_t rp = r4[0];
+          bool vp = v4[0];
+#pragma unroll
+          for (int k = 1; k < 4; ++k)
+            if (warp == k) { rp = r4[k]; vp = v4[k]; }
+          if (!bad) bad = !mbar_wait(bar_full(1), jj & 1, abort_flag, p.err);
+          if (!bad && vp) prefetch_l2_bulk(L.kv.base + (int64_t)rp * L.kv.row_stride, (uint32_t)p.d_qk * 2u);
+        }
       }
     } else if (warp == 4) {
       // ---------------------------------------------- query TMA + MMA issuer
@@ -425,15 +422,9 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       const int srow = quad * 32 + lane;  // key of S^T held by this lane
       const float c = L.scale * kLog2e;
       const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-      const int myblk = warp - 5;  // the column block this warp copies (if < NB-1)
-      auto copy_my_block = [&]() {
-        if (myblk < NB - 1)
-          copy_block(myblk, 0, std::integral_constant<int, 32>(), [&](int i) { return r4[i >> 3]; });
-      };
       if (my_tiles > 0) {
         resolve(0);
-        copy_my_block();
-        if (myblk < NB - 1) land(myblk < NB_A ? 0 : 1);
+        gather_last_block();
       }
       float lsum[32];
 #pragma unroll
@@ -441,10 +432,10 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       bool bad = false;
       for (int jj = 0; jj < my_tiles; ++jj) {
         const uint32_t par = jj & 1;
+        bad |= !mbar_wait(bar_valid, par, abort_flag, p.err);
         bad |= !mbar_wait(bar_s_full, par, abort_flag, p.err);
         tc_fence_after();
-        // this thread's key (row 32 quad + lane) resolved to a pool row
-        const bool kv = quad == 0 ? v4[0] : quad == 1 ? v4[1] : quad == 2 ? v4[2] : v4[3];
+        const bool kv = valid_s[srow] != 0;
         float x[32];
         auto load_scores = [&]() {
           uint32_t r[32];
@@ -526,14 +517,10 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
         tc_fence_before();
         mbar_arrive(bar_p_full);
         if (jj + 1 < my_tiles) {
-          // the next tile's column block `myblk` replaces this one once the PV
-          // MMAs that read it have completed
+          // the next tile's block NB-1 replaces this P^T once the PV has read it
           resolve(jj + 1);
-          if (myblk < NB - 1) {
-            bad |= !mbar_wait(bar_empty(myblk), jj & 1, abort_flag, p.err);
-            if (!bad) copy_my_block();
-            land(myblk < NB_A ? 0 : 1);
-          }
+          bad |= !mbar_wait(bar_empty(NB - 1), jj & 1, abort_flag, p.err);
+          if (!bad) gather_last_block();
         }
       }
       // l per head over this block's keys
@@ -689,7 +676,7 @@ template <int NB, int MB>
 cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   using C = MlaCfg<NB, MB>;
   auto kern = sparse_mla_kernel<NB, MB>;
-  CUtensorMap tq[DSA_MAX_LAYERS];
+  CUtensorMap tq[DSA_MAX_LAYERS], tc[DSA_MAX_LAYERS];
   for (int l = 0; l < DSA_MAX_LAYERS; ++l) {
     const int ls = l < a.n_layers ? l : 0;
     const MlaLayerView& lv = a.layer[ls];
@@ -698,6 +685,14 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
       const uint64_t strides[2] = {(uint64_t)a.d_qk * 2, (uint64_t)a.d_qk * lv.H * 2};
       const uint32_t box[3] = {64u, 64u, 1u};
       if (encode_tmap(&tq[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, lv.q, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+    {  // latent pool rows for tile::gather4: box of 64 dims x one row
+      const uint64_t dims[2] = {(uint64_t)a.d_qk, (uint64_t)lv.kv.num_rows};
+      const uint64_t strides[1] = {(uint64_t)lv.kv.row_stride * 2};
+      const uint32_t box[2] = {64u, 1u};
+      if (encode_tmap(&tc[l], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, lv.kv.base, dims, strides, box,
                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     }
@@ -742,7 +737,7 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   at[1] = pdl_attribute();
   cfg.attrs = at;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, tq[0], tq[1], tq[2], tq[3], p);
+  return cudaLaunchKernelEx(&cfg, kern, tq[0], tq[1], tq[2], tq[3], tc[0], tc[1], tc[2], tc[3], p);
 }
 
 }  // namespace
