@@ -63,7 +63,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 16.0f;  // move the reference only past 2^16
 constexpr int kSoftmaxThreads = 256;
 constexpr int kProducerThreads = 128;
-constexpr int kMaxSplit = 16;         // blocks per cluster (splits of one query's rows)
+constexpr int kMaxSplit = 8;          // blocks per cluster (splits of one query's rows)
 constexpr int kRows = 128;            // selected rows per tile
 constexpr int kBlk = kRows * 128;     // one [128 rows x 64 dims] bf16 block
 constexpr int kSlabHeader = 512;      // (m, l) x 64 heads, fp32
@@ -599,34 +599,24 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       // leave once all blocks have passed this point (the wait is at the end)
       if (csize > 1) cluster_arrive();
       // weight of each source per head: four threads per head, each with the
-      // sources sub, sub + 4, sub + 8, sub + 12; max and sum over a head's
-      // sources by shuffles
+      // sources sub and sub + 4; max and sum over a head's sources by shuffles
       {
         const int h = st >> 2, sub = st & 3;
-        float m[kMaxSplit / 4], l[kMaxSplit / 4];
-        float M = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit / 4; ++q) {
-          const int src = sub + 4 * q;
-          const float* hp = reinterpret_cast<const float*>(recv + src * slab_bytes);
-          m[q] = src < (int)csize ? hp[h] : -INFINITY;
-          l[q] = src < (int)csize ? hp[64 + h] : 0.f;
-          M = fmaxf(M, m[q]);
-        }
+        const float* h0p = reinterpret_cast<const float*>(recv + sub * slab_bytes);
+        const float* h1p = reinterpret_cast<const float*>(recv + (sub + 4) * slab_bytes);
+        const bool has0 = sub < (int)csize, has1 = sub + 4 < (int)csize;
+        const float m0 = has0 ? h0p[h] : -INFINITY, m1 = has1 ? h1p[h] : -INFINITY;
+        const float l0 = has0 ? h0p[64 + h] : 0.f, l1 = has1 ? h1p[64 + h] : 0.f;
+        float M = fmaxf(m0, m1);
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 1));
         M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
-        float Lsum = 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit / 4; ++q) {
-          m[q] = m[q] == -INFINITY ? 0.f : ex2_approx(m[q] - M);  // the source's factor
-          Lsum += l[q] * m[q];
-        }
+        const float e0 = m0 == -INFINITY ? 0.f : ex2_approx(m0 - M), e1 = m1 == -INFINITY ? 0.f : ex2_approx(m1 - M);
+        float Lsum = l0 * e0 + l1 * e1;
         Lsum += __shfl_xor_sync(0xffffffffu, Lsum, 1);
         Lsum += __shfl_xor_sync(0xffffffffu, Lsum, 2);
         const float inv = (ok && Lsum > 0.f) ? rcp_approx(Lsum) : 0.f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit / 4; ++q)
-          if (sub + 4 * q < (int)csize) f_s[(sub + 4 * q) * 64 + h] = m[q] * inv;
+        if (has0) f_s[sub * 64 + h] = e0 * inv;
+        if (has1) f_s[(sub + 4) * 64 + h] = e1 * inv;
         if (sub == 0 && crank == 0 && lo.lse != nullptr && h < lo.H)
           lo.lse[(int64_t)t * lo.H + h] = Lsum > 0.f ? (M + lg2_approx(Lsum)) * kLn2 : -INFINITY;
       }
@@ -718,11 +708,8 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   while (c * 2 <= std::min(max_cluster, kMaxSplit) && c * 2 <= tiles_max &&
          (int64_t)units * c * 2 <= a.num_sms)
     c *= 2;
-  // every block owns a value slice of >= 32 dims (one warp's lanes write one owner's slab),
-  // and the send and receive slabs of all blocks fit in the freed tile
-  while (c > 1 && ((a.d_v % (32 * c) != 0) ||
-                   2 * c * (kSlabHeader + (a.d_v / c) * 32 * 4) > C::STAGE))
-    c /= 2;
+  // every block owns a value slice of >= 32 dims (one warp's lanes write one owner's slab)
+  while (c > 1 && (a.d_v % (32 * c) != 0)) c /= 2;
 
   MlaParams p;
   for (int l = 0; l < DSA_MAX_LAYERS; ++l) p.layer[l] = a.layer[l < a.n_layers ? l : 0];
