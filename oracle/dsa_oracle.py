@@ -194,6 +194,24 @@ def dsa_forward(wl, queries: Optional[Sequence[int]] = None, layers: Optional[Se
     return res
 
 
+def cache_append(wl, pool: torch.Tensor, new_rows: torch.Tensor) -> torch.Tensor:
+    """A copy of `pool` with the row of every query token written in place.
+
+    Query token t of sequence b sits at position p_t; its row new_rows[t] goes
+    to the pool row that holds token p_t of b (page-table or contiguous
+    lookup), so that the token is part of its own causal context before the
+    indexer scores it (the top-k selector needs the full context in HBM: "How
+    GLM5.3 Sparse Attention Affects HBM Memory Usage", What it claims / Model).
+    Rows of other tokens are unchanged.
+    """
+    seq, pos = _query_table(wl)
+    out = pool.detach().clone()
+    for t, (b, p) in enumerate(zip(seq, pos)):
+        r = int(_rows_of(wl, b, np.array([p], dtype=np.int64))[0])
+        out[r] = new_rows[t]
+    return out
+
+
 def attention_on_set(wl, t: int, layer: int, sel: np.ndarray, kv_rows_fetch=None):
     """Sparse MLA of query t over an externally supplied index set `sel`
     (used to judge the GPU outputs on the GPU's own selection)."""

@@ -298,3 +298,58 @@ def test_workload_recipe():
     wr = W.make_workload(sp)
     allrows = torch.cat([W.pool_rows(wr, b, torch.arange(int(L))) for b, L in enumerate(wr.seq_lens.tolist())])
     assert torch.unique(allrows).numel() == allrows.numel()       # pages never overlap
+
+
+# ------------------------------------------------------------ cache append ---
+
+def _tiny_paged_workload():
+    # two sequences of 70 and 130 tokens, one query each (their last tokens),
+    # 64-token pages: sequence 0 on physical pages (2, 0), sequence 1 on (1, 3, 4)
+    spec = W.SPECS["ragged"].scaled(batch=2, ctx_range=(70, 130), topk=16, heads=2, d_qk=80, d_v=64,
+                                    idx_heads=4, idx_dim=32)
+    g = torch.Generator().manual_seed(5)
+    rows = 5 * 64
+    return W.Workload(spec=spec, seq_lens=torch.tensor([70, 130], dtype=torch.int32),
+                      cu_seqlens_q=torch.tensor([0, 1, 2], dtype=torch.int32),
+                      q_idx=torch.zeros((2, 4, 32), dtype=torch.bfloat16), w=torch.ones((2, 4)),
+                      k_idx=torch.randn((rows, 32), generator=g).to(torch.bfloat16),
+                      q=[torch.zeros((2, 2, 80), dtype=torch.bfloat16)],
+                      kv=[torch.randn((rows, 80), generator=g).to(torch.bfloat16)],
+                      page_table=torch.tensor([[2, 0, -1], [1, 3, 4]], dtype=torch.int32))
+
+
+def test_cache_append_hand_computed_rows():
+    # token 69 of sequence 0: page 1 -> physical 0, offset 5 -> row 5;
+    # token 129 of sequence 1: page 2 -> physical 4, offset 1 -> row 257
+    wl = _tiny_paged_workload()
+    new = torch.arange(2 * 32, dtype=torch.float32).reshape(2, 32).to(torch.bfloat16) + 1
+    out = oracle.cache_append(wl, wl.k_idx, new)
+    assert torch.equal(out[5], new[0]) and torch.equal(out[257], new[1])
+    keep = torch.ones(out.shape[0], dtype=torch.bool)
+    keep[[5, 257]] = False
+    assert torch.equal(out[keep], wl.k_idx[keep])
+
+
+@pytest.mark.parametrize("name,kw", [("decode", dict(ctx_len=700)), ("ragged", dict(ctx_range=(300, 900))),
+                                     ("prefill", dict(ctx_len=700, q_per_seq=9))])
+def test_cache_append_restores_the_generated_cache(name, kw):
+    # the workload generator placed every token's row; blanking the query
+    # tokens' rows and appending them again must give the generated pool back,
+    # and the forward must not change
+    spec = W.SPECS[name].scaled(batch=3, topk=128, heads=4, d_qk=80, d_v=64, idx_heads=4, idx_dim=32, **kw)
+    wl = W.make_workload(spec)
+    seq, pos = wl.query_positions()
+    at = torch.cat([W.pool_rows(wl, b, torch.tensor([p])) for b, p in zip(seq, pos)])
+    new_k, new_c = wl.k_idx[at].clone(), wl.kv[0][at].clone()
+    blank_k, blank_c = wl.k_idx.clone(), wl.kv[0].clone()
+    blank_k[at] = 0
+    blank_c[at] = 0
+    got_k = oracle.cache_append(wl, blank_k, new_k)
+    got_c = oracle.cache_append(wl, blank_c, new_c)
+    assert torch.equal(got_k, wl.k_idx) and torch.equal(got_c, wl.kv[0])
+    import dataclasses
+    again = dataclasses.replace(wl, k_idx=got_k, kv=[got_c])
+    a, b = oracle.dsa_forward(wl), oracle.dsa_forward(again)
+    for t in range(wl.total_q):
+        np.testing.assert_array_equal(a.idx[t], b.idx[t])
+        np.testing.assert_array_equal(a.out[0][t], b.out[0][t])
