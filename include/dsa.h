@@ -215,6 +215,27 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
                                 cudaStream_t stream, cudaEvent_t const* marks);
 
 /*
+ * Cache append: the rows of a batch's query tokens into a row cache, so that
+ * each new token is in its own causal context before the indexer scores it
+ * (the top-k selector reads the whole context from HBM: "How GLM5.3 Sparse
+ * Attention Affects HBM Memory Usage", What it claims / Model).  Call it once
+ * for the indexer keys and once per layer for the latent rows.
+ *   rows       device bf16 [total_q, ld_rows]: row t is query token t's new
+ *              row (its first row_elems elements are copied).
+ *   row_elems  multiple of 8, at most cache->row_stride; ld_rows >= row_elems,
+ *              multiple of 8.
+ *   cache      the pool is WRITTEN (through cache->base): query token t of
+ *              sequence b at position p_t goes to the row that holds token
+ *              p_t of b; no other row changes.  A page id out of range is
+ *              skipped and flagged DSA_ERR_BAD_INDEX.
+ *   workspace  device, >= dsa_workspace_size(batch, 0) bytes.
+ * IndexShare: the index set dsa_forward writes is the group's stored top-k;
+ * later layers of the group pass it to dsa_sparse_mla_fwd.
+ */
+dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_t ld_rows, int32_t row_elems,
+                              const dsa_cache_t* cache, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * dsa_sparse_mla_fwd_noalloc -- step 3 for callers that cannot provide any
  * device memory beyond their inputs and outputs (a plugin interface that
  * hands over only tensor pointers, or an engine whose device memory is all

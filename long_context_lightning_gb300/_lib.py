@@ -26,7 +26,7 @@ MAX_QUERIES = 65535
 
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
-           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster"]
+           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append"]
 NOALLOC_MAX_QUERIES = 4096
 
 
@@ -94,6 +94,9 @@ def load() -> ctypes.CDLL:
                                                c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_mma.restype = c_int32
     lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]
+    lib.dsa_cache_append.restype = c_int32
+    lib.dsa_cache_append.argtypes = [POINTER(Batch), c_void_p, c_int64, c_int32, POINTER(Cache), c_void_p, c_size_t,
+                                     c_void_p]
     lib.dsa_selftest_topk_max_cluster.restype = c_int32
     lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
     lib.dsa_selftest_timeout.restype = c_int32
@@ -219,6 +222,14 @@ def forward_marked(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaL
                                      idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream), ev),
            "dsa_forward_marked")
+
+
+def cache_append(batch: Batch, rows: torch.Tensor, cache: Cache, workspace: torch.Tensor, stream=None):
+    """Write row t of `rows` (bf16 [T, >= row width]) into `cache` at query token t's position."""
+    assert rows.dtype == torch.bfloat16 and rows.stride(1) == 1
+    _check(load().dsa_cache_append(ctypes.byref(batch), _ptr(rows), rows.stride(0), rows.shape[1],
+                                   ctypes.byref(cache), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                   _stream(stream)), "dsa_cache_append")
 
 
 def check_device_error(stream=None) -> int:

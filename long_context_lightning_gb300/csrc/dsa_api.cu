@@ -579,6 +579,32 @@ dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_t ld_rows, int32_t row_elems,
+                              const dsa_cache_t* cache, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_batch(batch);
+  if (s != DSA_OK) return s;
+  if (cache == nullptr || rows == nullptr || !aligned16(rows)) return DSA_ERR_INVALID_ARG;
+  if (row_elems < 8 || row_elems % 8 != 0 || ld_rows < row_elems || ld_rows % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if ((s = check_cache(*cache, row_elems, batch)) != DSA_OK) return s;
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < plan_bytes(batch->total_q))
+    return DSA_ERR_WORKSPACE;
+  if (batch->total_q == 0) return DSA_OK;
+  DeviceInfo dev;
+  if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
+  PlanView plan;
+  if ((s = run_plan(batch, 1, 0, workspace, dev, stream, &plan)) != DSA_OK) return s;
+  AppendLaunch a;
+  a.src = rows;
+  a.ld_src = ld_rows;
+  a.c = view_of(*cache);
+  a.row_elems = row_elems;
+  a.T = batch->total_q;
+  a.q_seq = plan.q_seq;
+  a.q_n = plan.q_n;
+  a.err = dev.err;
+  return launch_cache_append(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster) {
   if (max_cluster != 0 && max_cluster != 1 && max_cluster != 2 && max_cluster != 4 && max_cluster != 8 &&
       max_cluster != 16)

@@ -154,6 +154,18 @@ struct MlaLaunch {
 };
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
 
+struct AppendLaunch {
+  const void* src;    // bf16 [T, ld_src]
+  int64_t ld_src;
+  CacheView c;
+  int32_t row_elems;  // multiple of 8
+  int32_t T;
+  const int32_t* q_seq;
+  const int32_t* q_n;
+  int* err;
+};
+cudaError_t launch_cache_append(const AppendLaunch& a, cudaStream_t stream);
+
 // Largest thread-block cluster (8, or 16 where the device schedules it) for
 // kernel `kern` launched with `threads` threads and `smem` bytes of dynamic
 // shared memory, on the current device.  Probed once per (device, slot) under
