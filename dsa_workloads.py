@@ -17,6 +17,12 @@ Shapes and distributions follow the five workloads the library is measured on:
               64-token pages with a random page table.
   indexshare  2 decode queries at context 1048576, one indexer shared by 4
               layers, each layer with its own query and latent cache.
+  csa_flash   compressed entries (the compressed-sparse-attention layers of
+              the DeepSeek-V4 rows in "DeepSeek Sparse Attention", In the code):
+              32 decode queries at context 131072 tokens, one entry per 4
+              tokens (32768 entries), top-512 entries; indexer 64 x 128,
+              64-head MQA over 576-dim entries.
+  csa_pro     as csa_flash with top-1024 entries.
 
 The model shapes come from "How GLM5.3 Sparse Attention Affects HBM Memory
 Usage" (How it works / Model: 64 query heads, top-k 2048, dense below 2K;
@@ -64,6 +70,7 @@ class Spec:
     paged: bool = False
     page_size: int = 64
     integer_indexer: bool = False
+    compress_ratio: int = 1         # tokens per cache entry (1: one entry per token)
     idx_std: float = 1.0 / math.sqrt(128.0)
     w_std: float = 1.0 / 8.0
     kv_std: float = 0.05
@@ -89,6 +96,12 @@ SPECS = {
     "indexshare": Spec(name="indexshare", seed=4, batch=2, ctx_len=1048576, ctx_range=None, q_per_seq=1,
                        idx_heads=64, idx_dim=128, topk=2048, heads=64, d_qk=576, d_v=512,
                        scale=1.0 / 16.0, n_layers=4),
+    "csa_flash": Spec(name="csa_flash", seed=5, batch=32, ctx_len=131072, ctx_range=None, q_per_seq=1,
+                      idx_heads=64, idx_dim=128, topk=512, heads=64, d_qk=576, d_v=512,
+                      scale=1.0 / 16.0, compress_ratio=4),
+    "csa_pro": Spec(name="csa_pro", seed=6, batch=32, ctx_len=131072, ctx_range=None, q_per_seq=1,
+                    idx_heads=64, idx_dim=128, topk=1024, heads=64, d_qk=576, d_v=512,
+                    scale=1.0 / 16.0, compress_ratio=4),
 }
 
 
@@ -108,6 +121,9 @@ class Workload:
       seq_start    int64 [B]            contiguous: token s of b is row seq_start[b]+s
       page_table   int32 [B, P]         paged: token s of b is row
                                         page_table[b, s // page] * page + s % page
+    With spec.compress_ratio m > 1 the pools hold one entry per m tokens:
+    sequence b of L_b tokens has L_b // m entries (complete blocks), and
+    entry j takes the place of token s in the addressing above.
     """
     spec: Spec
     seq_lens: torch.Tensor
@@ -183,9 +199,11 @@ def make_workload(spec: Spec, device="cpu", kv_device=None) -> Workload:
     T = int(cu[-1])
 
     seq_start = page_table = None
+    # one pool row per cache entry: a token, or a block of compress_ratio tokens
+    n_rows = lens // spec.compress_ratio
     if spec.paged:
         ps = spec.page_size
-        npages = [(int(L) + ps - 1) // ps for L in lens.tolist()]
+        npages = [(int(L) + ps - 1) // ps for L in n_rows.tolist()]
         total_pages = sum(npages)
         perm = torch.randperm(total_pages, generator=_gen(spec, _T_PAGES, "cpu")).to(torch.int32)
         page_table = torch.full((B, max(npages)), -1, dtype=torch.int32)
@@ -196,8 +214,8 @@ def make_workload(spec: Spec, device="cpu", kv_device=None) -> Workload:
         rows = total_pages * ps
     else:
         seq_start = torch.zeros(B, dtype=torch.int64)
-        seq_start[1:] = torch.cumsum(lens.to(torch.int64), 0)[:-1]
-        rows = int(lens.to(torch.int64).sum())
+        seq_start[1:] = torch.cumsum(n_rows.to(torch.int64), 0)[:-1]
+        rows = int(n_rows.to(torch.int64).sum())
 
     if spec.integer_indexer:
         q_idx = torch.randint(-3, 4, (T, spec.idx_heads, spec.idx_dim), generator=_gen(spec, _T_QIDX, device),

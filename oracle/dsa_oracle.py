@@ -31,6 +31,15 @@ What is computed, and where it is defined:
                       the group attends over the same index set ("How GLM5.3
                       ...", How it works / IndexShare: every 4 DSA layers share
                       one indexer and the top-k indices are cached for reuse).
+  compressed entries  the same three steps over cache entries that each stand
+                      for m consecutive tokens, with top-512 or top-1024
+                      entries ("DeepSeek Sparse Attention", In the code: the
+                      DeepSeek-V4 indexers score compressed KV entries with
+                      ReLU(q.k) weighted sums and keep index_topk = 512 or
+                      1024).  Reading: entry j stands for tokens m j .. m j +
+                      m - 1 and is visible to a query at position p once its
+                      block is complete, so the query sees floor((p + 1) / m)
+                      entries.
 
 Readings where the pages are silent:
   * one indexer key per token, shared by all indexer heads;
@@ -169,7 +178,7 @@ def dsa_forward(wl, queries: Optional[Sequence[int]] = None, layers: Optional[Se
     k_pool = wl.k_idx
     for t in queries:
         b, p = seq[t], pos[t]
-        n = p + 1                                         # causal: s <= p
+        n = visible_entries(p, spec.compress_ratio)       # causal: s <= p (entries of complete blocks)
         if n <= spec.topk:
             sel = np.arange(n, dtype=np.int64)
         else:
@@ -228,11 +237,17 @@ def attention_on_set(wl, t: int, layer: int, sel: np.ndarray, kv_rows_fetch=None
     return sparse_mla(bf16_to_f64(wl.q[layer][t]), c, wl.spec.scale, wl.spec.d_v)
 
 
+def visible_entries(p: int, ratio: int) -> int:
+    """Cache entries a query at token position p sees: one per token (ratio 1),
+    or the complete blocks of `ratio` tokens."""
+    return (p + 1) // ratio
+
+
 def scores_for_query(wl, t: int) -> np.ndarray:
     """float64 indexer scores of query t over its whole causal context."""
     seq, pos = _query_table(wl)
     b, p = seq[t], pos[t]
-    rows = _rows_of(wl, b, np.arange(p + 1, dtype=np.int64))
+    rows = _rows_of(wl, b, np.arange(visible_entries(p, wl.spec.compress_ratio), dtype=np.int64))
     keys = bf16_to_f64(wl.k_idx[torch.from_numpy(rows).to(wl.k_idx.device)])
     return indexer_scores(bf16_to_f64(wl.q_idx[t]), f32_to_f64(wl.w[t]), keys)
 

@@ -63,7 +63,7 @@ def judge_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=N
     seq, pos = wl.query_positions()
     idx = idx.cpu().numpy()
     for t in queries:
-        n = pos[t] + 1
+        n = oracle.visible_entries(pos[t], spec.compress_ratio)
         row = idx[t]
         sel = sel_of(row)
         assert np.all(np.diff(sel) > 0), f"query {t}: selection not ascending/distinct"

@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import dsa_workloads as W
+import oracle
 from helpers import SeqKeys, judge_forward, make_sa
 
 pytestmark = pytest.mark.gpu
@@ -31,7 +32,7 @@ def _rows_valid(wl, idx):
     k = wl.spec.topk
     for t in range(idx.shape[0]):
         sel = idx[t][idx[t] >= 0]
-        n = pos[t] + 1
+        n = oracle.visible_entries(pos[t], wl.spec.compress_ratio)
         assert len(sel) == min(n, k), f"query {t}: {len(sel)} selected"
         assert np.all(np.diff(sel) > 0) and sel[0] >= 0 and sel[-1] < n, f"query {t}"
         assert np.all(idx[t][len(sel):] == -1)

@@ -353,3 +353,72 @@ def test_cache_append_restores_the_generated_cache(name, kw):
     for t in range(wl.total_q):
         np.testing.assert_array_equal(a.idx[t], b.idx[t])
         np.testing.assert_array_equal(a.out[0][t], b.out[0][t])
+
+
+# ------------------------------------------------------ compressed entries ---
+
+def test_compressed_entries_visible_by_brute_force():
+    # an entry is visible once every token of its block is at or before the
+    # query: enumerate blocks and tokens instead of using the floor formula
+    for ratio in (1, 2, 3, 4, 7):
+        for p in range(0, 40):
+            seen = 0
+            for j in range(0, 100):
+                if all(tok <= p for tok in range(ratio * j, ratio * j + ratio)):
+                    seen += 1
+            assert oracle.visible_entries(p, ratio) == seen
+
+
+def test_compressed_forward_equals_token_forward_on_the_same_rows():
+    # a cache of m-token entries whose entry j holds token j's row of an
+    # uncompressed cache: a query at token position m (p + 1) - 1 sees p + 1
+    # entries, exactly tokens 0..p of the uncompressed cache, so its selection
+    # and attention must equal the uncompressed query at position p
+    import dataclasses
+    m = 3
+    spec1 = W.SPECS["tiny"].scaled(ctx_len=300, q_per_seq=5, topk=64)
+    w1 = W.make_workload(spec1)
+    seq, pos = w1.query_positions()
+    specm = spec1.scaled(compress_ratio=m, ctx_len=m * 300)
+    wm = dataclasses.replace(w1, spec=specm, seq_lens=w1.seq_lens * m,
+                             cu_seqlens_q=w1.cu_seqlens_q)
+    # query i of wm sits at token position m*300 - 5 + i; shift the queries so
+    # that each lands at m (p + 1) - 1: rebuild with one query per sequence
+    a = oracle.dsa_forward(w1)
+    for t in range(w1.total_q):
+        p = pos[t]
+        wq = dataclasses.replace(wm, seq_lens=torch.tensor([m * (p + 1)], dtype=torch.int32),
+                                 cu_seqlens_q=torch.tensor([0, 1], dtype=torch.int32),
+                                 q_idx=w1.q_idx[t:t + 1], w=w1.w[t:t + 1], q=[w1.q[0][t:t + 1]])
+        bq = oracle.dsa_forward(wq)
+        np.testing.assert_array_equal(bq.idx[0], a.idx[t])
+        np.testing.assert_array_equal(bq.out[0][0], a.out[0][t])
+        np.testing.assert_array_equal(bq.lse[0][0], a.lse[0][t])
+
+
+def test_compressed_dense_when_entries_fit_top_k():
+    # k >= visible entries: every entry is attended, i.e. dense attention over
+    # the entries (torch's SDPA in float64)
+    spec = W.SPECS["tiny"].scaled(ctx_len=4 * 50, q_per_seq=3, topk=64, compress_ratio=4)
+    wl = W.make_workload(spec)
+    res = oracle.dsa_forward(wl)
+    assert res.indexer_calls == 0
+    seq, pos = wl.query_positions()
+    for t in range(wl.total_q):
+        n = (pos[t] + 1) // 4
+        np.testing.assert_array_equal(res.idx[t], np.arange(n))
+        rows = oracle.bf16_to_f64(wl.kv[0][:n])
+        ref = _sdpa_f64(oracle.bf16_to_f64(wl.q[0][t]), rows, spec.scale, spec.d_v)
+        np.testing.assert_allclose(res.out[0][t], ref, rtol=1e-11, atol=1e-13)
+
+
+def test_compressed_workload_layout():
+    for name in ("csa_flash", "csa_pro"):
+        spec = W.SPECS[name].scaled(batch=3, ctx_len=4000)
+        wl = W.make_workload(spec)
+        assert wl.k_idx.shape[0] == 3 * (4000 // spec.compress_ratio)
+        assert spec.topk in (512, 1024) and spec.idx_heads == 64 and spec.idx_dim == 128
+    ps = W.SPECS["csa_flash"].scaled(batch=4, ctx_len=None, ctx_range=(300, 5000), paged=True)
+    wp = W.make_workload(ps)
+    allrows = torch.cat([W.pool_rows(wp, b, torch.arange(int(L) // 4)) for b, L in enumerate(wp.seq_lens.tolist())])
+    assert torch.unique(allrows).numel() == allrows.numel()
