@@ -13,7 +13,8 @@ Under torchrun each rank runs its own 32-sequence batch (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
 
 Beside the decode headline, the line carries `per_config`: the tiny,
-chunked-prefill, ragged-paged and IndexShare workloads, each timed the same
+chunked-prefill, ragged-paged and IndexShare workloads and two compressed-entry
+workloads (top-512 and top-1024 of one entry per 4 tokens), each timed the same
 way (CUDA-graph replay of the fused call, CUDA events on the launching stream,
 L2 flushed between steps) with its dominant kernel's roofline and the oracle
 timed on a bounded sample beside it.  For IndexShare one query token is one
@@ -55,7 +56,9 @@ def _shape(wl):
     from long_context_lightning_gb300 import accounting
     s = wl.spec
     seq, pos = wl.query_positions()
-    return accounting.Shape(n=[p + 1 for p in pos], seq_of=seq, idx_heads=s.idx_heads, idx_dim=s.idx_dim,
+    # causal context in cache entries (tokens, or complete blocks of compress_ratio tokens)
+    return accounting.Shape(n=[(p + 1) // s.compress_ratio for p in pos], seq_of=seq, idx_heads=s.idx_heads,
+                            idx_dim=s.idx_dim,
                             topk=s.topk, heads=s.heads, d_qk=s.d_qk, d_v=s.d_v, n_layers=s.n_layers)
 
 
@@ -336,6 +339,8 @@ CPU_SAMPLE = {
     "prefill": (lambda T: [0, T // 2, T - 1, 1, T // 4, 3 * T // 4], "chunk queries at 0, T/4, T/2, 3T/4, T-1 and 1"),
     "ragged": (lambda T: list(range(T)), "ragged queries in order"),
     "indexshare": (lambda T: list(range(T)), "queries through all 4 layers"),
+    "csa_flash": (lambda T: list(range(T)), "decode queries over compressed entries, in order"),
+    "csa_pro": (lambda T: list(range(T)), "decode queries over compressed entries, in order"),
 }
 
 
@@ -461,7 +466,7 @@ def run_gpu(args, rank, world, local_rank):
 def _per_config(args, dev, stream, flush_l2, peaks):
     out = {}
     steps = max(3, min(args.steps, 20))
-    for name in ("tiny", "prefill", "ragged", "indexshare"):
+    for name in ("tiny", "prefill", "ragged", "indexshare", "csa_flash", "csa_pro"):
         spec = W.SPECS[name]
         run = _Run(spec, dev)
         step_ms = run.time_steps(steps, args.warmup, flush_l2, stream)
@@ -478,7 +483,8 @@ def _per_config(args, dev, stream, flush_l2, peaks):
         dt, nq = _oracle_sample(wl, queries, kv_on_device=(name == "indexshare"))
         out[name] = {
             "workload": _config(spec)["workload"] + (f", {spec.n_layers} layers" if spec.n_layers > 1 else "")
-                        + (", paged 64-token pages, lengths U{256..16384}" if spec.paged else ""),
+                        + (", paged 64-token pages, lengths U{256..16384}" if spec.paged else "")
+                        + (f", one cache entry per {spec.compress_ratio} tokens" if spec.compress_ratio > 1 else ""),
             "value": T / (ms * 1e-3), "unit": "query tokens/s" + (" (one query through the 4-layer group)"
                                                                    if spec.n_layers > 1 else ""),
             "ms_per_step": ms, "steps": steps, "kernels_ms": kern_ms, "roofline": roof,

@@ -203,6 +203,26 @@ dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
                          cudaStream_t stream);
 
 /*
+ * The fused forward over compressed cache entries ("DeepSeek Sparse
+ * Attention", In the code: the DeepSeek-V4 indexers score compressed KV
+ * entries with ReLU(q.k) weighted sums and keep the top index_topk = 512 or
+ * 1024 entries for compressed sparse attention).  Each cache row (indexer key
+ * and latent row alike) is one entry standing for compress_ratio consecutive
+ * tokens: entry j of sequence b covers tokens compress_ratio * j .. + ratio - 1
+ * and takes row seq_start[b] + j (contiguous) or page_table[b, j / 64] * 64 +
+ * j % 64 (paged, 64 entries a page).  seq_lens_k and max_seqlen_k still count
+ * TOKENS, and the queries are the last tokens of each sequence; a query at
+ * position p sees the (p + 1) / compress_ratio entries of complete blocks and
+ * selects the topk of them (all of them when they are at most topk).  idx
+ * holds entry indices.  Everything else as dsa_forward; the same workspace size
+ * serves.  compress_ratio 1 is dsa_forward.
+ */
+dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_ratio, const dsa_indexer_t* indexer,
+                                    int32_t topk, int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx,
+                                    int64_t ld_idx, void* const* outs, float* const* lses, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * dsa_forward with timing marks: identical work, plus cudaEventRecord of the
  * caller's events on `stream` -- marks[0] before the first launch, marks[1]
  * after the per-call plan, marks[2] after the indexer, marks[3] after the

@@ -26,7 +26,8 @@ MAX_QUERIES = 65535
 
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
-           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append"]
+           "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
+           "dsa_forward_compressed"]
 NOALLOC_MAX_QUERIES = 4096
 
 
@@ -94,6 +95,10 @@ def load() -> ctypes.CDLL:
                                                c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_mma.restype = c_int32
     lib.dsa_selftest_mma.argtypes = [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]
+    lib.dsa_forward_compressed.restype = c_int32
+    lib.dsa_forward_compressed.argtypes = [POINTER(Batch), c_int32, POINTER(Indexer), c_int32, c_int32,
+                                           POINTER(MlaLayer), c_void_p, c_int64, POINTER(c_void_p), POINTER(c_void_p),
+                                           c_void_p, c_size_t, c_void_p]
     lib.dsa_cache_append.restype = c_int32
     lib.dsa_cache_append.argtypes = [POINTER(Batch), c_void_p, c_int64, c_int32, POINTER(Cache), c_void_p, c_size_t,
                                      c_void_p]
@@ -197,8 +202,17 @@ def sparse_mla_fwd_noalloc(batch: Batch, layer: MlaLayer, idx: torch.Tensor, k: 
 
 def forward(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], idx: torch.Tensor,
             outs: Sequence[torch.Tensor], lses: Optional[Sequence[Optional[torch.Tensor]]],
-            workspace: torch.Tensor, stream=None):
+            workspace: torch.Tensor, stream=None, compress_ratio: int = 1):
     n = len(layers)
+    if compress_ratio != 1:
+        arr = (MlaLayer * n)(*layers)
+        out_ptrs = (c_void_p * n)(*[_ptr(o) for o in outs])
+        lse_ptrs = None if lses is None else (c_void_p * n)(*[_ptr(x) for x in lses])
+        _check(load().dsa_forward_compressed(ctypes.byref(batch), compress_ratio, ctypes.byref(indexer), k, n, arr,
+                                             _ptr(idx), idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _stream(stream)),
+               "dsa_forward_compressed")
+        return
     arr = (MlaLayer * n)(*layers)
     out_ptrs = (c_void_p * n)(*[_ptr(o) for o in outs])
     lse_ptrs = None if lses is None else (c_void_p * n)(*[_ptr(x) for x in lses])

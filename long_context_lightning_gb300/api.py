@@ -20,6 +20,7 @@ class SparseAttention:
     k_pool        bf16 [rows, d_I] indexer-key pool
     q_layers      per layer bf16 [T, H, D]; kv_pools per layer bf16 [rows, D]
     seq_start     int64 [B] (contiguous pools) or page_table int32 [B, P] (paged)
+    compress_ratio  tokens per cache entry (pools of compressed entries; 1: one row per token)
     """
 
     def __init__(self, cu_seqlens_q: torch.Tensor, seq_lens_k: torch.Tensor, q_idx: torch.Tensor,
@@ -27,9 +28,10 @@ class SparseAttention:
                  kv_pools: Sequence[torch.Tensor], d_v: int, scale: float, topk: int,
                  seq_start: Optional[torch.Tensor] = None, page_table: Optional[torch.Tensor] = None,
                  page_size: int = 64, total_q: Optional[int] = None, max_seqlen_k: Optional[int] = None,
-                 max_q_per_seq: Optional[int] = None, with_lse: bool = True):
+                 max_q_per_seq: Optional[int] = None, with_lse: bool = True, compress_ratio: int = 1):
         dev = q_idx.device
         self.topk = topk
+        self.compress_ratio = compress_ratio
         nq = (cu_seqlens_q[1:] - cu_seqlens_q[:-1])
         self.total_q = int(cu_seqlens_q[-1]) if total_q is None else total_q
         self.max_seqlen_k = int(seq_lens_k.max()) if max_seqlen_k is None else max_seqlen_k
@@ -54,13 +56,15 @@ class SparseAttention:
     def forward(self, stream=None):
         """indexer -> top-k -> sparse MLA for every layer; asynchronous on `stream`."""
         _lib.forward(self.batch, self.indexer, self.topk, self.layers, self.idx, self.outs, self.lses,
-                     self.workspace, stream)
+                     self.workspace, stream, compress_ratio=self.compress_ratio)
         return self.idx, self.outs, self.lses
 
     def scores_view(self) -> torch.Tensor:
-        """The fp32 score matrix the fused call leaves in its workspace ([T, ld])."""
-        from ._lib import MAX_TOPK  # noqa: F401
-        ld = (self.max_seqlen_k + 3) // 4 * 4
-        nbytes = self.total_q * ld * 4
-        off = self.workspace.numel() - nbytes
-        return self.workspace[off:].view(torch.float32).view(self.total_q, ld)
+        """The fp32 score matrix the fused call leaves in its workspace ([T, ld]).
+
+        The workspace holds the plan, then room for [T, round_up(max_seqlen_k, 4)]
+        fp32 scores; the fused call writes [T, round_up(max entries, 4)] there."""
+        ld_tokens = (self.max_seqlen_k + 3) // 4 * 4
+        ld = (self.max_seqlen_k // self.compress_ratio + 3) // 4 * 4
+        off = self.workspace.numel() - self.total_q * ld_tokens * 4
+        return self.workspace[off:off + self.total_q * ld * 4].view(torch.float32).view(self.total_q, ld)

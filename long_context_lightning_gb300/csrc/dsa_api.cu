@@ -68,7 +68,8 @@ dsa_status_t check_batch(const dsa_batch_t* b) {
   return DSA_OK;
 }
 
-dsa_status_t check_cache(const dsa_cache_t& c, int row_elems, const dsa_batch_t* b) {
+// `max_rows`: the most cache rows (tokens or entries) a sequence of the batch holds.
+dsa_status_t check_cache(const dsa_cache_t& c, int row_elems, int64_t max_rows) {
   if (c.base == nullptr || !aligned16(c.base)) return DSA_ERR_INVALID_ARG;
   if (c.row_stride < row_elems || c.row_stride % 8 != 0 || c.num_rows < 1) return DSA_ERR_INVALID_ARG;
   if (c.kind == DSA_CACHE_CONTIGUOUS) {
@@ -76,7 +77,7 @@ dsa_status_t check_cache(const dsa_cache_t& c, int row_elems, const dsa_batch_t*
   } else if (c.kind == DSA_CACHE_PAGED) {
     if (c.page_table == nullptr || !aligned4(c.page_table)) return DSA_ERR_INVALID_ARG;
     if (c.page_size != 64) return DSA_ERR_UNSUPPORTED;
-    if (c.page_table_stride < (b->max_seqlen_k + c.page_size - 1) / c.page_size) return DSA_ERR_INVALID_ARG;
+    if (c.page_table_stride < (max_rows + c.page_size - 1) / c.page_size) return DSA_ERR_INVALID_ARG;
   } else {
     return DSA_ERR_INVALID_ARG;
   }
@@ -97,23 +98,24 @@ CacheView view_of(const dsa_cache_t& c) {
   return v;
 }
 
-dsa_status_t check_indexer(const dsa_indexer_t* ix, const dsa_batch_t* b) {
+dsa_status_t check_indexer(const dsa_indexer_t* ix, const dsa_batch_t* b, int ratio = 1) {
   if (ix == nullptr || ix->q == nullptr || ix->w == nullptr || !aligned16(ix->q) || !aligned4(ix->w))
     return DSA_ERR_INVALID_ARG;
   if (ix->n_heads < 1 || ix->n_heads > 64) return DSA_ERR_UNSUPPORTED;
   if (ix->head_dim != 32 && ix->head_dim != 64 && ix->head_dim != 128) return DSA_ERR_UNSUPPORTED;
-  return check_cache(ix->k, ix->head_dim, b);
+  return check_cache(ix->k, ix->head_dim, b->max_seqlen_k / ratio);
 }
 
-dsa_status_t check_layer(const dsa_mla_layer_t* l, const dsa_batch_t* b) {
+dsa_status_t check_layer(const dsa_mla_layer_t* l, const dsa_batch_t* b, int ratio = 1) {
   if (l == nullptr || l->q == nullptr || !aligned16(l->q)) return DSA_ERR_INVALID_ARG;
   if (l->n_heads < 1 || l->n_heads > 64) return DSA_ERR_UNSUPPORTED;
   if (!((l->d_qk == 576 && l->d_v == 512) || (l->d_qk == 80 && l->d_v == 64))) return DSA_ERR_UNSUPPORTED;
   if (!(l->scale > 0.f) || l->scale != l->scale) return DSA_ERR_INVALID_ARG;
-  return check_cache(l->kv, l->d_qk, b);
+  return check_cache(l->kv, l->d_qk, b->max_seqlen_k / ratio);
 }
 
-size_t scores_ld(const dsa_batch_t* b) { return align_up((size_t)b->max_seqlen_k, 4); }
+// leading dimension of the score matrix: the most entries a query sees, rounded to 4
+size_t scores_ld(const dsa_batch_t* b, int ratio = 1) { return align_up((size_t)(b->max_seqlen_k / ratio), 4); }
 
 size_t forward_ws_bytes(const dsa_batch_t* b) {
   return align_up(plan_bytes(b->total_q), 256) + (size_t)b->total_q * scores_ld(b) * sizeof(float);
@@ -121,7 +123,7 @@ size_t forward_ws_bytes(const dsa_batch_t* b) {
 
 // Plan for this call: q_seq/q_n for every query and the indexer work list.
 dsa_status_t run_plan(const dsa_batch_t* b, int group, int skip_dense_k, void* ws, const DeviceInfo& dev,
-                      cudaStream_t stream, PlanView* out) {
+                      cudaStream_t stream, PlanView* out, int ratio = 1) {
   PlanParams pp;
   pp.cu_seqlens_q = b->cu_seqlens_q;
   pp.seq_lens_k = b->seq_lens_k;
@@ -130,6 +132,7 @@ dsa_status_t run_plan(const dsa_batch_t* b, int group, int skip_dense_k, void* w
   pp.max_seqlen_k = b->max_seqlen_k;
   pp.group = group;
   pp.skip_dense_k = skip_dense_k;
+  pp.ratio = ratio;
   pp.plan = plan_view(ws, b->total_q);
   pp.err = dev.err;
   *out = pp.plan;
@@ -158,7 +161,7 @@ dsa_status_t launch_indexer_call(const dsa_batch_t* b, const dsa_indexer_t* ix, 
 
 dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t ld, int32_t k, int32_t* idx,
                               int64_t ld_idx, const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream,
-                              bool plan_early = false) {
+                              bool plan_early = false, int ratio = 1) {
   TopkLaunch a;
   a.scores = scores;
   a.ld_scores = ld;
@@ -166,7 +169,7 @@ dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t
   a.ld_idx = ld_idx;
   a.k = k;
   a.T = b->total_q;
-  a.max_n = b->max_seqlen_k;
+  a.max_n = std::max(1, b->max_seqlen_k / ratio);
   a.q_n = plan.q_n;
   a.err = dev.err;
   a.num_sms = dev.num_sms;
@@ -177,7 +180,7 @@ dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t
 dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_layer_t* layers,
                              void* const* outs, float* const* lses, const int32_t* idx, int64_t ld_idx, int32_t k,
                              const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream,
-                             bool plan_early = false) {
+                             bool plan_early = false, int ratio = 1) {
   MlaLaunch a;
   std::memset(&a, 0, sizeof(a));
   for (int l = 0; l < n_layers; ++l) {
@@ -195,7 +198,7 @@ dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_l
   a.ld_idx = ld_idx;
   a.k = k;
   a.T = b->total_q;
-  a.max_n = b->max_seqlen_k;
+  a.max_n = std::max(1, b->max_seqlen_k / ratio);
   a.q_seq = plan.q_seq;
   a.q_n = plan.q_n;
   a.err = dev.err;
@@ -464,18 +467,24 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_batch_t* batch, const dsa_mla_layer_t*
   return launch_mla_call(batch, 1, layer, outs, lses, idx, ld_idx, topk, plan, dev, stream);
 }
 
-dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
-                                int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
-                                void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
-                                cudaStream_t stream, cudaEvent_t const* marks) {
+}  // extern "C"
+
+namespace dsa {
+namespace {
+// indexer -> top-k -> sparse MLA over cache entries of `ratio` tokens (1: tokens)
+dsa_status_t forward_impl(const dsa_batch_t* batch, int ratio, const dsa_indexer_t* indexer, int32_t topk,
+                          int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                          void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream, cudaEvent_t const* marks) {
   dsa_status_t s = check_batch(batch);
   if (s != DSA_OK) return s;
-  if ((s = check_indexer(indexer, batch)) != DSA_OK) return s;
+  if (ratio < 1 || ratio > batch->max_seqlen_k) return DSA_ERR_INVALID_ARG;
+  if ((s = check_indexer(indexer, batch, ratio)) != DSA_OK) return s;
   if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
   if (n_layers < 1 || n_layers > DSA_MAX_LAYERS || layers == nullptr || outs == nullptr) return DSA_ERR_INVALID_ARG;
   if ((int64_t)batch->total_q * n_layers > DSA_MAX_QUERIES) return DSA_ERR_UNSUPPORTED;
   for (int l = 0; l < n_layers; ++l) {
-    if ((s = check_layer(&layers[l], batch)) != DSA_OK) return s;
+    if ((s = check_layer(&layers[l], batch, ratio)) != DSA_OK) return s;
     if (layers[l].d_qk != layers[0].d_qk || layers[l].d_v != layers[0].d_v) return DSA_ERR_UNSUPPORTED;
     if (outs[l] == nullptr || !aligned16(outs[l])) return DSA_ERR_INVALID_ARG;
     if (lses != nullptr && lses[l] != nullptr && !aligned4(lses[l])) return DSA_ERR_INVALID_ARG;
@@ -489,19 +498,40 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
   auto mark = [&](int i) { return marks == nullptr || cudaEventRecord(marks[i], stream) == cudaSuccess; };
   if (!mark(0)) return DSA_ERR_CUDA;
   PlanView plan;
-  if ((s = run_plan(batch, indexer_group(batch), topk, workspace, dev, stream, &plan)) != DSA_OK) return s;
+  if ((s = run_plan(batch, indexer_group(batch), topk, workspace, dev, stream, &plan, ratio)) != DSA_OK) return s;
   if (!mark(1)) return DSA_ERR_CUDA;
   float* scores = reinterpret_cast<float*>(static_cast<char*>(workspace) + align_up(plan_bytes(batch->total_q), 256));
-  const int64_t ld = (int64_t)scores_ld(batch);
+  const int64_t ld = (int64_t)scores_ld(batch, ratio);
   if ((s = launch_indexer_call(batch, indexer, scores, ld, plan, dev, stream)) != DSA_OK) return s;
   if (!mark(2)) return DSA_ERR_CUDA;
   // the plan kernel ran two launches before the top-k and three before the MLA
-  if ((s = launch_topk_call(batch, scores, ld, topk, idx, ld_idx, plan, dev, stream, true)) != DSA_OK) return s;
+  if ((s = launch_topk_call(batch, scores, ld, topk, idx, ld_idx, plan, dev, stream, true, ratio)) != DSA_OK)
+    return s;
   if (!mark(3)) return DSA_ERR_CUDA;
-  if ((s = launch_mla_call(batch, n_layers, layers, outs, lses, idx, ld_idx, topk, plan, dev, stream, true)) !=
-      DSA_OK)
+  if ((s = launch_mla_call(batch, n_layers, layers, outs, lses, idx, ld_idx, topk, plan, dev, stream, true,
+                           ratio)) != DSA_OK)
     return s;
   return mark(4) ? DSA_OK : DSA_ERR_CUDA;
+}
+}  // namespace
+}  // namespace dsa
+
+extern "C" {
+
+dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
+                                int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                                void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream, cudaEvent_t const* marks) {
+  return forward_impl(batch, 1, indexer, topk, n_layers, layers, idx, ld_idx, outs, lses, workspace,
+                      workspace_bytes, stream, marks);
+}
+
+dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_ratio, const dsa_indexer_t* indexer,
+                                    int32_t topk, int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx,
+                                    int64_t ld_idx, void* const* outs, float* const* lses, void* workspace,
+                                    size_t workspace_bytes, cudaStream_t stream) {
+  return forward_impl(batch, compress_ratio, indexer, topk, n_layers, layers, idx, ld_idx, outs, lses, workspace,
+                      workspace_bytes, stream, nullptr);
 }
 
 dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk, int32_t n_layers,
@@ -585,7 +615,7 @@ dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_
   if (s != DSA_OK) return s;
   if (cache == nullptr || rows == nullptr || !aligned16(rows)) return DSA_ERR_INVALID_ARG;
   if (row_elems < 8 || row_elems % 8 != 0 || ld_rows < row_elems || ld_rows % 8 != 0) return DSA_ERR_INVALID_ARG;
-  if ((s = check_cache(*cache, row_elems, batch)) != DSA_OK) return s;
+  if ((s = check_cache(*cache, row_elems, batch->max_seqlen_k)) != DSA_OK) return s;
   if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < plan_bytes(batch->total_q))
     return DSA_ERR_WORKSPACE;
   if (batch->total_q == 0) return DSA_OK;

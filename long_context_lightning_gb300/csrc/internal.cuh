@@ -41,7 +41,8 @@ __device__ __forceinline__ int64_t cache_row(const CacheView& c, int b, int64_t 
 // ------------------------------------------------------------------ plan ---
 // Per-call plan written to the head of the workspace by plan_kernel:
 //   q_seq[T]  sequence of query t
-//   q_n[T]    causal context n_t = p_t + 1 (0 when its sequence is malformed)
+//   q_n[T]    causal context n_t = (p_t + 1) / ratio cache entries (one per token
+//             when ratio = 1; 0 when its sequence is malformed)
 //   groups    consecutive queries of one sequence scored together by the
 //             indexer (G per group): g_info[g] = {b, first query, #queries,
 //             n of the group's last query}, g_tile_start[g] = first 128-key
@@ -84,6 +85,7 @@ struct PlanParams {
   int32_t max_seqlen_k;
   int32_t group;        // G queries per indexer group
   int32_t skip_dense_k; // groups whose every query has n <= skip are given no work
+  int32_t ratio;        // tokens per cache entry: a query at position p sees (p + 1) / ratio entries
   PlanView plan;
   int* err;
 };

@@ -1,6 +1,7 @@
 // plan.cu -- per-call plan of a ragged batch: sequence and causal length of
-// every query token, and the indexer's flat list of (query group, 128-key
-// tile) work items.  One block; runs ahead of the compute kernels on the same
+// every query token (in cache entries: tokens, or complete blocks of `ratio`
+// tokens), and the indexer's flat list of (query group, 128-key tile) work
+// items.  One block; runs ahead of the compute kernels on the same
 // stream, so no host round trip is needed to size ragged work.  The batch's
 // two length arrays are staged in shared memory so every search is on-chip.
 #include "internal.cuh"
@@ -104,7 +105,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
     const bool ok = seq_ok(p, sa, lo, &nq, &len);
     const int i = t - cu_s[lo];
     p.plan.q_seq[t] = lo;
-    p.plan.q_n[t] = (ok && i >= 0 && i < nq) ? (len - nq + i + 1) : 0;
+    p.plan.q_n[t] = (ok && i >= 0 && i < nq) ? (len - nq + i + 1) / p.ratio : 0;
   }
 
   // (3) every group: its queries and its number of 128-key work items
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kPlanThreads, 1) plan_kernel(PlanParams p) {
       seq_ok(p, sa, b, &nq, &len);
       const int q0 = cu_s[b] + j * G;
       const int cnt = min(G, nq - j * G);
-      const int n_last = len - nq + j * G + cnt;  // causal n of the group's last query
+      const int n_last = (len - nq + j * G + cnt) / p.ratio;  // causal n (entries) of the group's last query
       p.plan.g_info[g] = make_int4(b, q0, cnt, n_last);
       items = (n_last > p.skip_dense_k) ? (n_last + kIdxTileKeys - 1) / kIdxTileKeys : 0;
     }

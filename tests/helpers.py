@@ -17,7 +17,7 @@ def make_sa(wl, with_lse=True):
     s = wl.spec
     return SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, s.d_v, s.scale,
                            s.topk, seq_start=wl.seq_start, page_table=wl.page_table, page_size=s.page_size,
-                           with_lse=with_lse)
+                           with_lse=with_lse, compress_ratio=s.compress_ratio)
 
 
 def sel_of(row: np.ndarray) -> np.ndarray:
