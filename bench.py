@@ -221,7 +221,7 @@ class _Run:
         wl = self.wl
         self.sa = SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, spec.d_v,
                                   spec.scale, spec.topk, seq_start=wl.seq_start, page_table=wl.page_table,
-                                  page_size=spec.page_size)
+                                  page_size=spec.page_size, compress_ratio=spec.compress_ratio)
         self.sa.forward()
         torch.cuda.synchronize(dev)
         status = _lib.check_device_error()
@@ -265,7 +265,7 @@ class _Run:
         for i in range(n):
             flush_l2(i)
             _lib.forward_marked(sa.batch, sa.indexer, sa.topk, sa.layers, sa.idx, sa.outs, sa.lses, sa.workspace,
-                                marks[i])
+                                marks[i], compress_ratio=self.spec.compress_ratio)
         torch.cuda.synchronize(self.dev)
         per = {k: [] for k in KERNELS}
         for m in marks:

@@ -214,13 +214,14 @@ dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
  * TOKENS, and the queries are the last tokens of each sequence; a query at
  * position p sees the (p + 1) / compress_ratio entries of complete blocks and
  * selects the topk of them (all of them when they are at most topk).  idx
- * holds entry indices.  Everything else as dsa_forward; the same workspace size
- * serves.  compress_ratio 1 is dsa_forward.
+ * holds entry indices.  Everything else as dsa_forward (`marks`: NULL, or five
+ * timing events as in dsa_forward_marked); the same workspace size serves.
+ * compress_ratio 1 is dsa_forward.
  */
 dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_ratio, const dsa_indexer_t* indexer,
                                     int32_t topk, int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx,
                                     int64_t ld_idx, void* const* outs, float* const* lses, void* workspace,
-                                    size_t workspace_bytes, cudaStream_t stream);
+                                    size_t workspace_bytes, cudaStream_t stream, cudaEvent_t const* marks);
 
 /*
  * dsa_forward with timing marks: identical work, plus cudaEventRecord of the

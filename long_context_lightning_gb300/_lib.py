@@ -98,7 +98,7 @@ def load() -> ctypes.CDLL:
     lib.dsa_forward_compressed.restype = c_int32
     lib.dsa_forward_compressed.argtypes = [POINTER(Batch), c_int32, POINTER(Indexer), c_int32, c_int32,
                                            POINTER(MlaLayer), c_void_p, c_int64, POINTER(c_void_p), POINTER(c_void_p),
-                                           c_void_p, c_size_t, c_void_p]
+                                           c_void_p, c_size_t, c_void_p, POINTER(c_void_p)]
     lib.dsa_cache_append.restype = c_int32
     lib.dsa_cache_append.argtypes = [POINTER(Batch), c_void_p, c_int64, c_int32, POINTER(Cache), c_void_p, c_size_t,
                                      c_void_p]
@@ -210,7 +210,7 @@ def forward(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], 
         lse_ptrs = None if lses is None else (c_void_p * n)(*[_ptr(x) for x in lses])
         _check(load().dsa_forward_compressed(ctypes.byref(batch), compress_ratio, ctypes.byref(indexer), k, n, arr,
                                              _ptr(idx), idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
-                                             workspace.numel() * workspace.element_size(), _stream(stream)),
+                                             workspace.numel() * workspace.element_size(), _stream(stream), None),
                "dsa_forward_compressed")
         return
     arr = (MlaLayer * n)(*layers)
@@ -222,7 +222,8 @@ def forward(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], 
 
 
 def forward_marked(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], idx: torch.Tensor,
-                   outs: Sequence[torch.Tensor], lses, workspace: torch.Tensor, marks: Sequence, stream=None):
+                   outs: Sequence[torch.Tensor], lses, workspace: torch.Tensor, marks: Sequence, stream=None,
+                   compress_ratio: int = 1):
     """forward() that also records the 5 torch.cuda.Event `marks` between its launches."""
     n = len(layers)
     arr = (MlaLayer * n)(*layers)
@@ -232,6 +233,12 @@ def forward_marked(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaL
     if not all(handles):
         raise ValueError("record each torch.cuda.Event once before passing it (torch creates it lazily)")
     ev = (c_void_p * 5)(*handles)
+    if compress_ratio != 1:
+        _check(load().dsa_forward_compressed(ctypes.byref(batch), compress_ratio, ctypes.byref(indexer), k, n, arr,
+                                             _ptr(idx), idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _stream(stream), ev),
+               "dsa_forward_compressed")
+        return
     _check(load().dsa_forward_marked(ctypes.byref(batch), ctypes.byref(indexer), k, n, arr, _ptr(idx),
                                      idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
                                      workspace.numel() * workspace.element_size(), _stream(stream), ev),

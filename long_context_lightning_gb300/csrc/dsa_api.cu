@@ -529,9 +529,9 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
 dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_ratio, const dsa_indexer_t* indexer,
                                     int32_t topk, int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx,
                                     int64_t ld_idx, void* const* outs, float* const* lses, void* workspace,
-                                    size_t workspace_bytes, cudaStream_t stream) {
+                                    size_t workspace_bytes, cudaStream_t stream, cudaEvent_t const* marks) {
   return forward_impl(batch, compress_ratio, indexer, topk, n_layers, layers, idx, ld_idx, outs, lses, workspace,
-                      workspace_bytes, stream, nullptr);
+                      workspace_bytes, stream, marks);
 }
 
 dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk, int32_t n_layers,
