@@ -221,6 +221,65 @@ def cache_append(wl, pool: torch.Tensor, new_rows: torch.Tensor) -> torch.Tensor
     return out
 
 
+class HiSparseLRU:
+    """HBM as a least-recently-used cache of latent rows over host memory
+    ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
+    HiSparse (SGLang): rows chosen by top-k that are missing from HBM are
+    loaded from host DRAM; cold rows are evicted back to DRAM).
+
+    `order` lists the resident rows, least recently used first.  One step takes
+    the rows a batch selected (first-request order, repeats ignored):
+      * hits are the requested rows already resident, misses the others;
+      * the least recently used rows that this step does not request are
+        evicted, as many as the misses need (the cache is read-only, so an
+        evicted row needs no write-back: host memory holds every row);
+      * every requested row becomes most recent: the hits in their previous
+        order, then the misses in request order.
+    Readings where the pages are silent: the requested rows of one step must
+    all fit (capacity >= distinct rows of the step), and rows used in the same
+    step keep their relative order as stated above.
+    """
+
+    def __init__(self, capacity: int):
+        from collections import OrderedDict
+        self.capacity = capacity
+        self.order = OrderedDict()
+
+    def step(self, requested):
+        want = list(dict.fromkeys(int(r) for r in requested))
+        want_set = set(want)
+        if len(want) > self.capacity:
+            raise ValueError("a step requests more distinct rows than the cache holds")
+        hits = [r for r in want if r in self.order]
+        misses = [r for r in want if r not in self.order]
+        n_evict = max(0, len(self.order) + len(misses) - self.capacity)
+        evicted = []
+        for r in self.order:                       # least recently used first
+            if len(evicted) == n_evict:
+                break
+            if r not in want_set:
+                evicted.append(r)
+        for r in evicted:
+            del self.order[r]
+        for r in [r for r in self.order if r in want_set]:
+            self.order.move_to_end(r)               # hits, previous relative order
+        for r in misses:
+            self.order[r] = None                    # then the misses, in request order
+        return hits, misses, evicted
+
+
+def requested_rows(wl, idx_rows) -> list:
+    """Pool rows a batch's selection requests, in (query, slot) order: query t's
+    row of positions idx_rows[t] (entries < 0 skipped), first occurrences kept."""
+    seq, pos = _query_table(wl)
+    out = []
+    for t in range(len(seq)):
+        sel = np.asarray(idx_rows[t], dtype=np.int64)
+        sel = sel[sel >= 0]
+        out.extend(int(r) for r in _rows_of(wl, seq[t], sel))
+    return list(dict.fromkeys(out))
+
+
 def attention_on_set(wl, t: int, layer: int, sel: np.ndarray, kv_rows_fetch=None):
     """Sparse MLA of query t over an externally supplied index set `sel`
     (used to judge the GPU outputs on the GPU's own selection)."""

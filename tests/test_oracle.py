@@ -422,3 +422,59 @@ def test_compressed_workload_layout():
     wp = W.make_workload(ps)
     allrows = torch.cat([W.pool_rows(wp, b, torch.arange(int(L) // 4)) for b, L in enumerate(wp.seq_lens.tolist())])
     assert torch.unique(allrows).numel() == allrows.numel()
+
+
+# ------------------------------------------------------- HiSparse LRU cache ---
+
+def test_lru_hand_worked_trace():
+    with open(os.path.join(GOLDEN, "lru_trace.json")) as f:
+        g = json.load(f)
+    c = oracle.HiSparseLRU(g["capacity"])
+    for st in g["steps"]:
+        hits, misses, evicted = c.step(st["request"])
+        assert hits == st["hits"] and misses == st["misses"] and evicted == st["evicted"], st
+        assert list(c.order) == st["order_after"], st
+
+
+def test_lru_closed_forms():
+    r = np.random.default_rng(3)
+    # capacity >= every row ever requested: nothing is evicted, a request hits
+    # exactly when the row was requested before
+    c = oracle.HiSparseLRU(1000)
+    seen = set()
+    for _ in range(30):
+        req = r.choice(200, size=40, replace=False).tolist()
+        hits, misses, evicted = c.step(req)
+        assert evicted == [] and set(hits) == set(req) & seen and set(misses) == set(req) - seen
+        seen |= set(req)
+    # capacity = request size and disjoint requests: every step misses
+    # everything and evicts the whole previous step
+    c = oracle.HiSparseLRU(50)
+    prev = []
+    for s in range(6):
+        req = list(range(50 * s, 50 * s + 50))
+        hits, misses, evicted = c.step(req)
+        assert hits == [] and misses == req and sorted(evicted) == sorted(prev)
+        prev = req
+
+
+def test_lru_invariants_on_random_traces():
+    r = np.random.default_rng(4)
+    for cap in (16, 40, 100):
+        c = oracle.HiSparseLRU(cap)
+        last_use = {}
+        for s in range(60):
+            req = r.choice(150, size=int(r.integers(1, 16)), replace=True).tolist()
+            before = set(c.order)
+            hits, misses, evicted = c.step(req)
+            want = set(req)
+            assert want <= set(c.order) and len(c.order) <= cap
+            assert set(hits) == want & before and set(misses) == want - before
+            assert not (set(evicted) & want)
+            # no evicted row was used more recently than a kept row that this
+            # step did not request
+            kept_old = set(c.order) - want
+            if evicted and kept_old:
+                assert max(last_use[e] for e in evicted) <= min(last_use[k] for k in kept_old)
+            for x in want:
+                last_use[x] = s
