@@ -67,10 +67,11 @@ typedef enum {
   DSA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required */
   DSA_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   DSA_ERR_TIMEOUT = 5,      /* a bounded device-side wait ran out */
-  DSA_ERR_BAD_INDEX = 6     /* a device-side length, page id or index was out of range */
+  DSA_ERR_BAD_INDEX = 6,    /* a device-side length, page id or index was out of range */
+  DSA_ERR_CAPACITY = 7      /* a device-side capacity was exceeded (HiSparse: rows of one step > slots) */
 } dsa_status_t;
 
-typedef enum { DSA_CACHE_CONTIGUOUS = 0, DSA_CACHE_PAGED = 1 } dsa_cache_kind_t;
+typedef enum { DSA_CACHE_CONTIGUOUS = 0, DSA_CACHE_PAGED = 1, DSA_CACHE_ROWS = 2 } dsa_cache_kind_t;
 
 /*
  * A per-token row cache (indexer keys, or MLA latent rows) held in one pool of
@@ -79,6 +80,8 @@ typedef enum { DSA_CACHE_CONTIGUOUS = 0, DSA_CACHE_PAGED = 1 } dsa_cache_kind_t;
  *   paged:      token s of sequence b is row
  *                 page_table[b * page_table_stride + s / page_size] * page_size
  *                 + s % page_size.
+ *   rows:       a position IS a pool row (no sequence addressing; sparse MLA
+ *               only, e.g. over the HBM slots a HiSparse fetch returns).
  * Pages of a sequence beyond ceil(seq_lens_k[b] / page_size) are never read.
  */
 typedef struct {
@@ -136,7 +139,8 @@ const char* dsa_status_string(dsa_status_t status);
 /*
  * Synchronises `stream`, then reads and clears the device error word set by
  * earlier kernels of this library on the current device.  Returns DSA_OK,
- * DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT, or DSA_ERR_CUDA if the sync failed.
+ * DSA_ERR_BAD_INDEX, DSA_ERR_TIMEOUT, DSA_ERR_CAPACITY, or DSA_ERR_CUDA if the
+ * sync failed.
  */
 dsa_status_t dsa_check_device_error(cudaStream_t stream);
 
@@ -255,6 +259,64 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
  */
 dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_t ld_rows, int32_t row_elems,
                               const dsa_cache_t* cache, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * HiSparse: HBM as a least-recently-used cache of one layer's latent rows over
+ * host memory ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it
+ * works / HiSparse (SGLang): rows chosen by top-k that are missing from HBM are
+ * loaded from host DRAM, cold rows are evicted, the loads for layer N overlap
+ * layer N-1).  The latent pool lives in host memory that the device can read
+ * (pinned or registered host memory); `capacity` rows of it are held in a
+ * device slot pool.  The cache is read-only: evicting a row drops it (host
+ * memory keeps every row).  All buffers are caller-owned.
+ */
+typedef struct {
+  int32_t capacity;     /* device slots (rows the HBM cache holds) */
+  int32_t row_elems;    /* elements of a cached row (the latent width), multiple of 8 */
+  void* slot_pool;      /* device bf16 [capacity, slot_stride] */
+  int64_t slot_stride;  /* elements between slots, multiple of 8, >= row_elems */
+  int64_t host_rows;    /* rows of the host pool (= the host cache's num_rows) */
+  void* state;          /* device, >= dsa_hisparse_state_bytes(capacity, host_rows) bytes */
+} dsa_hisparse_t;
+
+/* Bytes of the device state of a cache (0 on invalid sizes). */
+size_t dsa_hisparse_state_bytes(int32_t capacity, int64_t host_rows);
+
+/* Empties the cache (every slot free, step counter 0).  Call once before the first fetch. */
+dsa_status_t dsa_hisparse_reset(const dsa_hisparse_t* hs, cudaStream_t stream);
+
+/*
+ * One step: makes every row a batch selected resident and returns where.
+ *   host_cache  the layer's latent cache in host memory: contiguous or paged
+ *               addressing as for dsa_sparse_mla_fwd, base readable by the
+ *               device, num_rows = hs->host_rows.
+ *   idx         the selection, as for dsa_sparse_mla_fwd (entries j <
+ *               min(topk, n_t); -1 entries skipped, bad ones flagged).
+ *   slots       device int32 [total_q, ld_slots]: entry j of row t is the slot
+ *               of idx[t, j]'s row, -1 where idx is -1 (and for j >= min(topk,
+ *               n_t)).  Pass it to dsa_sparse_mla_fwd with a cache of kind
+ *               DSA_CACHE_ROWS over slot_pool (num_rows = capacity).
+ * Policy: the distinct requested rows in first-request order (row t, then
+ * entry j); hits are resident, misses are copied from host memory into the
+ * slots of the least recently used rows this step does not request; every
+ * requested row becomes most recent (hits in their previous order, then the
+ * misses in request order).  If the distinct rows of one step exceed
+ * capacity, nothing changes, the error word reports DSA_ERR_CAPACITY and the
+ * missing entries of `slots` are -1.
+ * workspace: device, >= dsa_workspace_size(batch, 0) bytes.
+ */
+dsa_status_t dsa_hisparse_fetch(const dsa_hisparse_t* hs, const dsa_batch_t* batch, const dsa_cache_t* host_cache,
+                                const int32_t* idx, int64_t ld_idx, int32_t topk, int32_t* slots, int64_t ld_slots,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* The host rows held by the cache, least recently used first: rows[i] for the
+ * i-th slot of the LRU order, -1 for a free slot.  rows: device int32 [capacity]. */
+dsa_status_t dsa_hisparse_resident(const dsa_hisparse_t* hs, int32_t* rows, cudaStream_t stream);
+
+/* Counters of the last fetch, copied to the host (synchronises `stream`):
+ * stats[0] steps so far, [1] distinct rows requested, [2] hits, [3] misses
+ * (rows loaded), [4] rows evicted, [5] 1 if the capacity was exceeded. */
+dsa_status_t dsa_hisparse_stats(const dsa_hisparse_t* hs, int32_t* stats, cudaStream_t stream);
 
 /*
  * dsa_sparse_mla_fwd_noalloc -- step 3 for callers that cannot provide any

@@ -2,9 +2,10 @@
 
 The compute path is libdsa.so (hand-written CUDA for sm_103a, C ABI in
 include/dsa.h): lightning indexer -> exact top-k -> sparse MLA in MQA mode,
-with IndexShare reuse of one index set across a group of layers.
+with IndexShare reuse of one index set across a group of layers, and an
+HBM least-recently-used cache of latent rows over pinned host memory.
 """
 from . import _lib
-from .api import SparseAttention
+from .api import HiSparseCache, SparseAttention
 
-__all__ = ["SparseAttention", "_lib"]
+__all__ = ["SparseAttention", "HiSparseCache", "_lib"]

@@ -18,8 +18,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_WORKSPACE, DSA_ERR_CUDA, DSA_ERR_TIMEOUT, \
-    DSA_ERR_BAD_INDEX = range(7)
-CACHE_CONTIGUOUS, CACHE_PAGED = 0, 1
+    DSA_ERR_BAD_INDEX, DSA_ERR_CAPACITY = range(8)
+CACHE_CONTIGUOUS, CACHE_PAGED, CACHE_ROWS = 0, 1, 2
 MAX_TOPK = 2048
 MAX_LAYERS = 4
 MAX_QUERIES = 65535
@@ -27,7 +27,8 @@ MAX_QUERIES = 65535
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
            "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
-           "dsa_forward_compressed"]
+           "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_reset", "dsa_hisparse_fetch",
+           "dsa_hisparse_resident", "dsa_hisparse_stats"]
 NOALLOC_MAX_QUERIES = 4096
 
 
@@ -49,6 +50,11 @@ class Indexer(ctypes.Structure):
 class MlaLayer(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("kv", Cache), ("n_heads", c_int32), ("d_qk", c_int32), ("d_v", c_int32),
                 ("scale", c_float)]
+
+
+class HiSparse(ctypes.Structure):
+    _fields_ = [("capacity", c_int32), ("row_elems", c_int32), ("slot_pool", c_void_p), ("slot_stride", c_int64),
+                ("host_rows", c_int64), ("state", c_void_p)]
 
 
 class DsaError(RuntimeError):
@@ -104,6 +110,17 @@ def load() -> ctypes.CDLL:
                                      c_void_p]
     lib.dsa_selftest_topk_max_cluster.restype = c_int32
     lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
+    lib.dsa_hisparse_state_bytes.restype = c_size_t
+    lib.dsa_hisparse_state_bytes.argtypes = [c_int32, c_int64]
+    lib.dsa_hisparse_reset.restype = c_int32
+    lib.dsa_hisparse_reset.argtypes = [POINTER(HiSparse), c_void_p]
+    lib.dsa_hisparse_fetch.restype = c_int32
+    lib.dsa_hisparse_fetch.argtypes = [POINTER(HiSparse), POINTER(Batch), POINTER(Cache), c_void_p, c_int64, c_int32,
+                                       c_void_p, c_int64, c_void_p, c_size_t, c_void_p]
+    lib.dsa_hisparse_resident.restype = c_int32
+    lib.dsa_hisparse_resident.argtypes = [POINTER(HiSparse), c_void_p, c_void_p]
+    lib.dsa_hisparse_stats.restype = c_int32
+    lib.dsa_hisparse_stats.argtypes = [POINTER(HiSparse), POINTER(c_int32), c_void_p]
     lib.dsa_selftest_timeout.restype = c_int32
     lib.dsa_selftest_timeout.argtypes = [c_int32, c_void_p]
     _lib = lib
@@ -148,6 +165,12 @@ def make_cache(pool: torch.Tensor, seq_start: Optional[torch.Tensor] = None,
                      page_table.shape[1])
     assert seq_start is not None and seq_start.dtype == torch.int64
     return Cache(CACHE_CONTIGUOUS, 0, _ptr(pool), pool.stride(0), pool.shape[0], _ptr(seq_start), None, 0)
+
+
+def make_rows_cache(pool: torch.Tensor) -> Cache:
+    """Cache whose selection entries are pool rows themselves (a HiSparse slot pool)."""
+    assert pool.dtype == torch.bfloat16 and pool.dim() == 2 and pool.stride(1) == 1
+    return Cache(CACHE_ROWS, 0, _ptr(pool), pool.stride(0), pool.shape[0], None, None, 0)
 
 
 def make_indexer(q_idx: torch.Tensor, w: torch.Tensor, k_cache: Cache) -> Indexer:
@@ -251,6 +274,42 @@ def cache_append(batch: Batch, rows: torch.Tensor, cache: Cache, workspace: torc
     _check(load().dsa_cache_append(ctypes.byref(batch), _ptr(rows), rows.stride(0), rows.shape[1],
                                    ctypes.byref(cache), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                    _stream(stream)), "dsa_cache_append")
+
+
+def hisparse_state_bytes(capacity: int, host_rows: int) -> int:
+    return int(load().dsa_hisparse_state_bytes(capacity, host_rows))
+
+
+def make_hisparse(slot_pool: torch.Tensor, host_rows: int, state: torch.Tensor) -> HiSparse:
+    """Descriptor of an HBM row cache: bf16 [capacity, width] slot pool plus a state buffer."""
+    assert slot_pool.dtype == torch.bfloat16 and slot_pool.dim() == 2 and slot_pool.stride(1) == 1
+    return HiSparse(slot_pool.shape[0], slot_pool.shape[1], _ptr(slot_pool), slot_pool.stride(0), host_rows,
+                    _ptr(state))
+
+
+def hisparse_reset(hs: HiSparse, stream=None):
+    _check(load().dsa_hisparse_reset(ctypes.byref(hs), _stream(stream)), "dsa_hisparse_reset")
+
+
+def hisparse_fetch(hs: HiSparse, batch: Batch, host_cache: Cache, idx: torch.Tensor, k: int, slots: torch.Tensor,
+                   workspace: torch.Tensor, stream=None):
+    assert idx.dtype == torch.int32 and idx.stride(1) == 1
+    assert slots.dtype == torch.int32 and slots.stride(1) == 1
+    _check(load().dsa_hisparse_fetch(ctypes.byref(hs), ctypes.byref(batch), ctypes.byref(host_cache), _ptr(idx),
+                                     idx.stride(0), k, _ptr(slots), slots.stride(0), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dsa_hisparse_fetch")
+
+
+def hisparse_resident(hs: HiSparse, rows: torch.Tensor, stream=None):
+    assert rows.dtype == torch.int32 and rows.is_contiguous() and rows.numel() >= hs.capacity
+    _check(load().dsa_hisparse_resident(ctypes.byref(hs), _ptr(rows), _stream(stream)), "dsa_hisparse_resident")
+
+
+def hisparse_stats(hs: HiSparse, stream=None) -> list:
+    out = (c_int32 * 8)()
+    _check(load().dsa_hisparse_stats(ctypes.byref(hs), out, _stream(stream)), "dsa_hisparse_stats")
+    return list(out)
 
 
 def check_device_error(stream=None) -> int:

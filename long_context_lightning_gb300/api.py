@@ -68,3 +68,49 @@ class SparseAttention:
         ld = (self.max_seqlen_k // self.compress_ratio + 3) // 4 * 4
         off = self.workspace.numel() - self.total_q * ld_tokens * 4
         return self.workspace[off:off + self.total_q * ld * 4].view(torch.float32).view(self.total_q, ld)
+
+
+class HiSparseCache:
+    """HBM slot pool holding the most recently used rows of one layer's latent
+    pool, which lives in pinned host memory.
+
+    fetch() makes every row a selection asks for resident (misses copied from
+    host memory, least recently used rows that the step does not ask for
+    evicted) and writes the slot of each selected entry; layer() gives the
+    sparse-MLA descriptor that reads those slots.  The host pool keeps its
+    addressing (seq_start or page_table, as for SparseAttention).
+    """
+
+    def __init__(self, host_pool: torch.Tensor, capacity: int, seq_start: Optional[torch.Tensor] = None,
+                 page_table: Optional[torch.Tensor] = None, page_size: int = 64, device=None):
+        if not host_pool.is_pinned():
+            raise ValueError("the host pool must be pinned host memory (tensor.pin_memory())")
+        device = torch.device("cuda") if device is None else torch.device(device)
+        self.host_pool = host_pool
+        self.host_cache = _lib.make_cache(host_pool, seq_start, page_table, page_size)
+        self.slot_pool = torch.empty((capacity, host_pool.shape[1]), dtype=torch.bfloat16, device=device)
+        self.state = torch.empty(_lib.hisparse_state_bytes(capacity, host_pool.shape[0]), dtype=torch.uint8,
+                                 device=device)
+        self.hs = _lib.make_hisparse(self.slot_pool, host_pool.shape[0], self.state)
+        self.rows_cache = _lib.make_rows_cache(self.slot_pool)
+        self._keep = [seq_start, page_table]
+        _lib.hisparse_reset(self.hs)
+
+    def fetch(self, batch, idx: torch.Tensor, k: int, slots: torch.Tensor, workspace: torch.Tensor, stream=None):
+        """Asynchronous on `stream`: slots[t, j] = slot of idx[t, j]'s row (-1 where idx is -1)."""
+        _lib.hisparse_fetch(self.hs, batch, self.host_cache, idx, k, slots, workspace, stream)
+        return slots
+
+    def layer(self, q: torch.Tensor, d_v: int, scale: float):
+        """Sparse-MLA layer descriptor over the slot pool (pass the slots as its index set)."""
+        return _lib.make_layer(q, self.rows_cache, d_v, scale)
+
+    def resident(self) -> List[int]:
+        """Resident host rows, least recently used first."""
+        rows = torch.empty(self.hs.capacity, dtype=torch.int32, device=self.slot_pool.device)
+        _lib.hisparse_resident(self.hs, rows)
+        return [r for r in rows.cpu().tolist() if r >= 0]
+
+    def stats(self) -> dict:
+        s = _lib.hisparse_stats(self.hs)
+        return dict(steps=s[0], requested=s[1], hits=s[2], misses=s[3], evicted=s[4], overflow=s[5])

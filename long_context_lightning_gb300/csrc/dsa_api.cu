@@ -78,6 +78,8 @@ dsa_status_t check_cache(const dsa_cache_t& c, int row_elems, int64_t max_rows) 
     if (c.page_table == nullptr || !aligned4(c.page_table)) return DSA_ERR_INVALID_ARG;
     if (c.page_size != 64) return DSA_ERR_UNSUPPORTED;
     if (c.page_table_stride < (max_rows + c.page_size - 1) / c.page_size) return DSA_ERR_INVALID_ARG;
+  } else if (c.kind == DSA_CACHE_ROWS) {
+    // positions are pool rows: nothing to check beyond the pool itself
   } else {
     return DSA_ERR_INVALID_ARG;
   }
@@ -95,12 +97,14 @@ CacheView view_of(const dsa_cache_t& c) {
   v.pt_stride = c.page_table_stride;
   v.page_size = c.page_size;
   v.paged = c.kind == DSA_CACHE_PAGED;
+  v.rows = c.kind == DSA_CACHE_ROWS;
   return v;
 }
 
 dsa_status_t check_indexer(const dsa_indexer_t* ix, const dsa_batch_t* b, int ratio = 1) {
   if (ix == nullptr || ix->q == nullptr || ix->w == nullptr || !aligned16(ix->q) || !aligned4(ix->w))
     return DSA_ERR_INVALID_ARG;
+  if (ix->k.kind == DSA_CACHE_ROWS) return DSA_ERR_UNSUPPORTED;  // the indexer scores a sequence's tokens
   if (ix->n_heads < 1 || ix->n_heads > 64) return DSA_ERR_UNSUPPORTED;
   if (ix->head_dim != 32 && ix->head_dim != 64 && ix->head_dim != 128) return DSA_ERR_UNSUPPORTED;
   return check_cache(ix->k, ix->head_dim, b->max_seqlen_k / ratio);
@@ -387,6 +391,7 @@ const char* dsa_status_string(dsa_status_t s) {
     case DSA_ERR_CUDA: return "DSA_ERR_CUDA: a CUDA call or launch failed";
     case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT: a bounded device-side wait ran out";
     case DSA_ERR_BAD_INDEX: return "DSA_ERR_BAD_INDEX: a device-side length, page id or index was out of range";
+    case DSA_ERR_CAPACITY: return "DSA_ERR_CAPACITY: a device-side capacity was exceeded";
   }
   return "DSA_ERR_UNKNOWN";
 }
@@ -401,6 +406,7 @@ dsa_status_t dsa_check_device_error(cudaStream_t stream) {
   if (cudaMemcpyToSymbol(g_dsa_error_word, &zero, sizeof(int)) != cudaSuccess) return DSA_ERR_CUDA;
   if (word & DEV_ERR_TIMEOUT) return DSA_ERR_TIMEOUT;
   if (word & DEV_ERR_BAD_INDEX) return DSA_ERR_BAD_INDEX;
+  if (word & DEV_ERR_CAPACITY) return DSA_ERR_CAPACITY;
   return DSA_OK;
 }
 
@@ -633,6 +639,94 @@ dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_
   a.q_n = plan.q_n;
   a.err = dev.err;
   return launch_cache_append(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+size_t dsa_hisparse_state_bytes(int32_t capacity, int64_t host_rows) {
+  if (capacity < 1 || host_rows < 1) return 0;
+  return hisparse_state_bytes(capacity, host_rows);
+}
+
+static dsa_status_t check_hisparse(const dsa_hisparse_t* hs) {
+  if (hs == nullptr || hs->capacity < 1 || hs->host_rows < 1 || hs->host_rows > (int64_t)0x7fffffff)
+    return DSA_ERR_INVALID_ARG;
+  if (hs->row_elems < 8 || hs->row_elems % 8 != 0 || hs->slot_stride < hs->row_elems || hs->slot_stride % 8 != 0)
+    return DSA_ERR_INVALID_ARG;
+  if (hs->slot_pool == nullptr || !aligned16(hs->slot_pool) || hs->state == nullptr || !aligned16(hs->state))
+    return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_hisparse_reset(const dsa_hisparse_t* hs, cudaStream_t stream) {
+  dsa_status_t s = check_hisparse(hs);
+  if (s != DSA_OK) return s;
+  return launch_hisparse_reset(hs->state, hs->capacity, hs->host_rows, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status_t dsa_hisparse_fetch(const dsa_hisparse_t* hs, const dsa_batch_t* batch, const dsa_cache_t* host_cache,
+                                const int32_t* idx, int64_t ld_idx, int32_t topk, int32_t* slots, int64_t ld_slots,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_batch(batch);
+  if (s != DSA_OK) return s;
+  if ((s = check_hisparse(hs)) != DSA_OK) return s;
+  if (host_cache == nullptr || host_cache->kind == DSA_CACHE_ROWS || host_cache->num_rows != hs->host_rows)
+    return DSA_ERR_INVALID_ARG;
+  if ((s = check_cache(*host_cache, hs->row_elems, batch->max_seqlen_k)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (idx == nullptr || !aligned4(idx) || ld_idx < topk) return DSA_ERR_INVALID_ARG;
+  if (slots == nullptr || !aligned4(slots) || ld_slots < topk) return DSA_ERR_INVALID_ARG;
+  if ((int64_t)batch->total_q * topk > (int64_t)0x7fffffff) return DSA_ERR_UNSUPPORTED;
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < plan_bytes(batch->total_q))
+    return DSA_ERR_WORKSPACE;
+  if (batch->total_q == 0) return DSA_OK;
+  DeviceInfo dev;
+  if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
+  PlanView plan;
+  if ((s = run_plan(batch, 1, 0, workspace, dev, stream, &plan)) != DSA_OK) return s;
+  // the host pool must be memory the device can read: pinned or registered
+  // host memory (its device address is used), or device / managed memory
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, host_cache->base) != cudaSuccess) {
+    cudaGetLastError();
+    return DSA_ERR_INVALID_ARG;
+  }
+  if (attr.type == cudaMemoryTypeUnregistered || attr.devicePointer == nullptr) return DSA_ERR_INVALID_ARG;
+  dsa_cache_t host = *host_cache;
+  host.base = attr.devicePointer;
+  HisparseLaunch a;
+  a.state = hs->state;
+  a.capacity = hs->capacity;
+  a.host_rows = hs->host_rows;
+  a.row_elems = hs->row_elems;
+  a.slot_pool = hs->slot_pool;
+  a.slot_stride = hs->slot_stride;
+  a.host = view_of(host);
+  a.idx = idx;
+  a.ld_idx = ld_idx;
+  a.k = topk;
+  a.T = batch->total_q;
+  a.q_seq = plan.q_seq;
+  a.q_n = plan.q_n;
+  a.slots = slots;
+  a.ld_slots = ld_slots;
+  a.err = dev.err;
+  return launch_hisparse_fetch(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+dsa_status_t dsa_hisparse_resident(const dsa_hisparse_t* hs, int32_t* rows, cudaStream_t stream) {
+  dsa_status_t s = check_hisparse(hs);
+  if (s != DSA_OK) return s;
+  if (rows == nullptr || !aligned4(rows)) return DSA_ERR_INVALID_ARG;
+  return launch_hisparse_resident(hs->state, hs->capacity, hs->host_rows, rows, stream) == cudaSuccess
+             ? DSA_OK
+             : DSA_ERR_CUDA;
+}
+
+dsa_status_t dsa_hisparse_stats(const dsa_hisparse_t* hs, int32_t* stats, cudaStream_t stream) {
+  dsa_status_t s = check_hisparse(hs);
+  if (s != DSA_OK) return s;
+  if (stats == nullptr) return DSA_ERR_INVALID_ARG;
+  return hisparse_read_stats(hs->state, hs->capacity, hs->host_rows, stats, stream) == cudaSuccess ? DSA_OK
+                                                                                                  : DSA_ERR_CUDA;
 }
 
 dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster) {

@@ -22,12 +22,15 @@ struct CacheView {
   int64_t pt_stride;
   int32_t page_size;
   int32_t paged;
+  int32_t rows;  // positions are pool rows (no sequence addressing)
 };
 
 // Pool row of token s of sequence b, or -1 when the page id / row is out of range.
 __device__ __forceinline__ int64_t cache_row(const CacheView& c, int b, int64_t s) {
   int64_t row;
-  if (c.paged) {
+  if (c.rows) {
+    row = s;
+  } else if (c.paged) {
     const int64_t page = s / c.page_size;
     const int64_t phys = __ldg(c.page_table + (int64_t)b * c.pt_stride + page);
     row = phys * c.page_size + (s - page * c.page_size);
@@ -167,6 +170,31 @@ struct AppendLaunch {
   int* err;
 };
 cudaError_t launch_cache_append(const AppendLaunch& a, cudaStream_t stream);
+
+struct HisparseLaunch {
+  void* state;
+  int32_t capacity;
+  int64_t host_rows;
+  int32_t row_elems;
+  void* slot_pool;
+  int64_t slot_stride;
+  CacheView host;
+  const int32_t* idx;
+  int64_t ld_idx;
+  int32_t k;
+  int32_t T;
+  const int32_t* q_seq;
+  const int32_t* q_n;
+  int32_t* slots;
+  int64_t ld_slots;
+  int* err;
+};
+size_t hisparse_state_bytes(int64_t capacity, int64_t host_rows);
+cudaError_t launch_hisparse_reset(void* state, int32_t capacity, int64_t host_rows, cudaStream_t stream);
+cudaError_t launch_hisparse_fetch(const HisparseLaunch& a, cudaStream_t stream);
+cudaError_t launch_hisparse_resident(void* state, int32_t capacity, int64_t host_rows, int32_t* rows,
+                                     cudaStream_t stream);
+cudaError_t hisparse_read_stats(void* state, int32_t capacity, int64_t host_rows, int32_t* out8, cudaStream_t stream);
 
 // Largest thread-block cluster (8, or 16 where the device schedules it) for
 // kernel `kern` launched with `threads` threads and `smem` bytes of dynamic

@@ -12,7 +12,7 @@ namespace dsa {
 
 // ---------------------------------------------------------------- errors ---
 // Bits of the device error word (a __device__ int owned by the library).
-enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_INDEX = 2 };
+enum : int { DEV_ERR_TIMEOUT = 1, DEV_ERR_BAD_INDEX = 2, DEV_ERR_CAPACITY = 4 };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s

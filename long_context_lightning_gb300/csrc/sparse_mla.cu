@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
     auto read_plan = [&]() {
       n_t = __ldcg(p.q_n + t);
       b = __ldcg(p.q_seq + t);
-      if (!L.kv.paged && b >= 0) seq_base = __ldg(L.kv.seq_start + b);
+      if (!L.kv.paged && !L.kv.rows && b >= 0) seq_base = __ldg(L.kv.seq_start + b);
     };
     if (p.plan_early) read_plan();
     pdl_wait();  // positions and plan of the previous grids are complete from here on
@@ -286,13 +286,14 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
       for (int k = 0; k < 4; ++k) {
         const int e = (j0 + jj) * kRows + 4 * lane + k;
         int pos = e < nvalid ? __ldg(idx_row + e) : -1;
-        if (pos >= n_t || pos < -1) {
+        // a position is a token of the sequence, or a pool row for a cache of rows
+        if ((!L.kv.rows && pos >= n_t) || pos < -1) {
           if (warp == 0) atomicOr(p.err, DEV_ERR_BAD_INDEX);
           pos = -1;
         }
         int64_t row = -1;
         if (pos >= 0) {
-          if (L.kv.paged) {
+          if (L.kv.paged || L.kv.rows) {
             row = cache_row(L.kv, b, pos);
           } else {
             row = seq_base + pos;
