@@ -18,7 +18,9 @@ workloads (top-512 and top-1024 of one entry per 4 tokens), each timed the same
 way (CUDA-graph replay of the fused call, CUDA events on the launching stream,
 L2 flushed between steps) with its dominant kernel's roofline and the oracle
 timed on a bounded sample beside it.  For IndexShare one query token is one
-query through the whole 4-layer group.
+query through the whole 4-layer group.  `per_config.hisparse` times the HBM
+row cache over pinned host memory on the decode workload (cold, warm and
+decode-like steps) and sparse MLA over its slots.
 """
 from __future__ import annotations
 
@@ -434,6 +436,7 @@ def run_gpu(args, rank, world, local_rank):
     per_config = {}
     if not args.no_per_config:
         per_config = _per_config(args, dev, stream, flush_l2, peaks)
+        per_config["hisparse"] = _hisparse(args, dev, stream, flush_l2)
 
     line = {
         "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world, "steps": args.steps,
@@ -498,6 +501,99 @@ def _per_config(args, dev, stream, flush_l2, peaks):
         del wl
         torch.cuda.empty_cache()
     return out
+
+
+def _hisparse(args, dev, stream, flush_l2):
+    """HiSparse on the decode workload: layer 0's latent pool (32 x 32768 rows)
+    in pinned host memory, an HBM slot pool of 262144 rows (a quarter of it).
+    Timed with CUDA events on the launching stream, L2 flushed before each:
+      cold   the indexer's selection into an empty cache (every row a miss)
+      warm   the same selection again (every row a hit)
+      step   a chain of selections, each replacing 1/8 of the previous one's
+             entries by random positions (the next decode step's top-k overlaps
+             the previous one), after the cold fill
+    and sparse MLA over the slots beside sparse MLA over the device pool."""
+    import oracle
+    from long_context_lightning_gb300 import HiSparseCache, _lib
+    spec = W.SPECS["decode"]
+    run = _Run(spec, dev)
+    wl, sa = run.wl, run.sa
+    T, k = wl.total_q, spec.topk
+    capacity = 262144
+    host = wl.kv[0].cpu().pin_memory()
+    hc = HiSparseCache(host, capacity, seq_start=wl.seq_start)
+    slots = torch.empty((T, k), dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(spec.seed * 1000 + 77)
+    n = (wl.seq_lens.to(torch.int64)).view(T, 1)          # one query per sequence, at its last position
+    chain = [sa.idx.clone()]
+    for _ in range(8):
+        nxt = chain[-1].clone()
+        fresh = (torch.rand((T, k), generator=g, device=dev) * n).to(torch.int32)
+        nxt[:, ::8] = fresh[:, ::8]
+        chain.append(nxt)
+    ev = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+
+    def timed(fn):
+        a, b = ev(), ev()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) * 1e3
+
+    cold, warm, step, step_miss = [], [], [], []
+    for rep_i in range(3):
+        _lib.hisparse_reset(hc.hs)
+        flush_l2(rep_i)
+        cold.append(timed(lambda: hc.fetch(sa.batch, chain[0], k, slots)))
+        cold_stats = hc.stats()
+        flush_l2(rep_i)
+        warm.append(timed(lambda: hc.fetch(sa.batch, chain[0], k, slots)))
+        for sel in chain[1:]:
+            flush_l2(rep_i)
+            step.append(timed(lambda: hc.fetch(sa.batch, sel, k, slots)))
+            step_miss.append(hc.stats()["misses"])
+    run.check("hisparse")
+    # sparse MLA over the slots (the last selection) and over the device pool
+    hc.fetch(sa.batch, chain[-1], k, slots)
+    layer_slots = hc.layer(wl.q[0], spec.d_v, spec.scale)
+    out = torch.empty_like(sa.outs[0])
+    lse = torch.empty_like(sa.lses[0])
+    mla_slots, mla_pool = [], []
+    for i in range(5):
+        flush_l2(i)
+        mla_slots.append(timed(lambda: _lib.sparse_mla_fwd(sa.batch, layer_slots, slots, k, out, lse,
+                                                           sa.workspace)))
+        flush_l2(i)
+        mla_pool.append(timed(lambda: _lib.sparse_mla_fwd(sa.batch, sa.layers[0], chain[-1], k, out, lse,
+                                                          sa.workspace)))
+    run.check("hisparse sparse MLA")
+    # the oracle's LRU bookkeeping on the same trace (host cores)
+    wl_cpu = wl.to("cpu", kv_too=False)
+    reqs = [oracle.requested_rows(wl_cpu, [r.numpy() for r in sel.cpu()]) for sel in chain]
+    lru = oracle.HiSparseLRU(capacity)
+    t0 = time.perf_counter()
+    for r in reqs:
+        lru.step(r)
+    dt = time.perf_counter() - t0
+    row_bytes = spec.d_qk * 2
+    cold_us = statistics.median(cold)
+    del run, hc, host
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"decode B={spec.batch} x ctx {spec.ctx_len}: layer-0 latent pool ({spec.batch * spec.ctx_len}"
+                    f" rows x {row_bytes} B) in pinned host memory, HBM slot pool of {capacity} rows",
+        "cold_fetch_us": cold_us, "cold_misses": cold_stats["misses"],
+        "cold_host_to_hbm_GBps": cold_stats["misses"] * row_bytes / (cold_us * 1e-6) / 1e9,
+        "warm_fetch_us": statistics.median(warm),
+        "step_fetch_us": statistics.median(step), "step_misses_mean": statistics.mean(step_miss),
+        "sparse_mla_over_slots_us": statistics.median(mla_slots),
+        "sparse_mla_over_pool_us": statistics.median(mla_pool),
+        "launches_per_fetch": 7,
+        "cpu_baseline": {"value": sum(len(r) for r in reqs) / dt, "unit": "requested rows/s", "kind": "oracle",
+                         "cores": 1, "sample": f"LRU bookkeeping of the {len(reqs)}-step trace, python, {dt:.2f} s"},
+    }
 
 
 def main():

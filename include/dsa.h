@@ -282,6 +282,9 @@ typedef struct {
 /* Bytes of the device state of a cache (0 on invalid sizes). */
 size_t dsa_hisparse_state_bytes(int32_t capacity, int64_t host_rows);
 
+/* Workspace bytes of dsa_hisparse_fetch for this batch, top-k and capacity (0 on invalid arguments). */
+size_t dsa_hisparse_workspace_size(const dsa_batch_t* batch, int32_t topk, int32_t capacity);
+
 /* Empties the cache (every slot free, step counter 0).  Call once before the first fetch. */
 dsa_status_t dsa_hisparse_reset(const dsa_hisparse_t* hs, cudaStream_t stream);
 
@@ -303,7 +306,11 @@ dsa_status_t dsa_hisparse_reset(const dsa_hisparse_t* hs, cudaStream_t stream);
  * misses in request order).  If the distinct rows of one step exceed
  * capacity, nothing changes, the error word reports DSA_ERR_CAPACITY and the
  * missing entries of `slots` are -1.
- * workspace: device, >= dsa_workspace_size(batch, 0) bytes.
+ * workspace: device, >= dsa_hisparse_workspace_size(batch, topk, capacity)
+ * bytes, not shared with a call that may run at the same time (a fetch for
+ * layer N on one stream beside layer N-1's attention on another needs its own).
+ * Fetches of one cache run in stream order; a fetch and a sparse-MLA call
+ * reading the same slots must be ordered by the caller (events or one stream).
  */
 dsa_status_t dsa_hisparse_fetch(const dsa_hisparse_t* hs, const dsa_batch_t* batch, const dsa_cache_t* host_cache,
                                 const int32_t* idx, int64_t ld_idx, int32_t topk, int32_t* slots, int64_t ld_slots,

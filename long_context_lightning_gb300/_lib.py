@@ -27,7 +27,7 @@ MAX_QUERIES = 65535
 EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", "dsa_indexer_scores",
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
            "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
-           "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_reset", "dsa_hisparse_fetch",
+           "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_workspace_size", "dsa_hisparse_reset", "dsa_hisparse_fetch",
            "dsa_hisparse_resident", "dsa_hisparse_stats"]
 NOALLOC_MAX_QUERIES = 4096
 
@@ -112,6 +112,8 @@ def load() -> ctypes.CDLL:
     lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
     lib.dsa_hisparse_state_bytes.restype = c_size_t
     lib.dsa_hisparse_state_bytes.argtypes = [c_int32, c_int64]
+    lib.dsa_hisparse_workspace_size.restype = c_size_t
+    lib.dsa_hisparse_workspace_size.argtypes = [POINTER(Batch), c_int32, c_int32]
     lib.dsa_hisparse_reset.restype = c_int32
     lib.dsa_hisparse_reset.argtypes = [POINTER(HiSparse), c_void_p]
     lib.dsa_hisparse_fetch.restype = c_int32
@@ -278,6 +280,10 @@ def cache_append(batch: Batch, rows: torch.Tensor, cache: Cache, workspace: torc
 
 def hisparse_state_bytes(capacity: int, host_rows: int) -> int:
     return int(load().dsa_hisparse_state_bytes(capacity, host_rows))
+
+
+def hisparse_workspace_size(batch: Batch, k: int, capacity: int) -> int:
+    return int(load().dsa_hisparse_workspace_size(ctypes.byref(batch), k, capacity))
 
 
 def make_hisparse(slot_pool: torch.Tensor, host_rows: int, state: torch.Tensor) -> HiSparse:

@@ -94,10 +94,18 @@ class HiSparseCache:
         self.hs = _lib.make_hisparse(self.slot_pool, host_pool.shape[0], self.state)
         self.rows_cache = _lib.make_rows_cache(self.slot_pool)
         self._keep = [seq_start, page_table]
+        self._ws: Optional[torch.Tensor] = None
         _lib.hisparse_reset(self.hs)
 
-    def fetch(self, batch, idx: torch.Tensor, k: int, slots: torch.Tensor, workspace: torch.Tensor, stream=None):
-        """Asynchronous on `stream`: slots[t, j] = slot of idx[t, j]'s row (-1 where idx is -1)."""
+    def fetch(self, batch, idx: torch.Tensor, k: int, slots: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+              stream=None):
+        """Asynchronous on `stream`: slots[t, j] = slot of idx[t, j]'s row (-1 where idx is -1).
+        Without `workspace` the cache keeps one of its own (grown as needed)."""
+        if workspace is None:
+            need = _lib.hisparse_workspace_size(batch, k, self.hs.capacity)
+            if self._ws is None or self._ws.numel() < need:
+                self._ws = torch.empty(need, dtype=torch.uint8, device=self.slot_pool.device)
+            workspace = self._ws
         _lib.hisparse_fetch(self.hs, batch, self.host_cache, idx, k, slots, workspace, stream)
         return slots
 

@@ -646,6 +646,11 @@ size_t dsa_hisparse_state_bytes(int32_t capacity, int64_t host_rows) {
   return hisparse_state_bytes(capacity, host_rows);
 }
 
+size_t dsa_hisparse_workspace_size(const dsa_batch_t* batch, int32_t topk, int32_t capacity) {
+  if (check_batch(batch) != DSA_OK || topk < 1 || topk > DSA_MAX_TOPK || capacity < 1) return 0;
+  return plan_bytes(batch->total_q) + hisparse_counts_bytes((int64_t)batch->total_q * topk, capacity);
+}
+
 static dsa_status_t check_hisparse(const dsa_hisparse_t* hs) {
   if (hs == nullptr || hs->capacity < 1 || hs->host_rows < 1 || hs->host_rows > (int64_t)0x7fffffff)
     return DSA_ERR_INVALID_ARG;
@@ -675,7 +680,8 @@ dsa_status_t dsa_hisparse_fetch(const dsa_hisparse_t* hs, const dsa_batch_t* bat
   if (idx == nullptr || !aligned4(idx) || ld_idx < topk) return DSA_ERR_INVALID_ARG;
   if (slots == nullptr || !aligned4(slots) || ld_slots < topk) return DSA_ERR_INVALID_ARG;
   if ((int64_t)batch->total_q * topk > (int64_t)0x7fffffff) return DSA_ERR_UNSUPPORTED;
-  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < plan_bytes(batch->total_q))
+  if (workspace == nullptr || !aligned16(workspace) ||
+      workspace_bytes < dsa_hisparse_workspace_size(batch, topk, hs->capacity))
     return DSA_ERR_WORKSPACE;
   if (batch->total_q == 0) return DSA_OK;
   DeviceInfo dev;
@@ -694,6 +700,7 @@ dsa_status_t dsa_hisparse_fetch(const dsa_hisparse_t* hs, const dsa_batch_t* bat
   host.base = attr.devicePointer;
   HisparseLaunch a;
   a.state = hs->state;
+  a.counts = static_cast<char*>(workspace) + plan_bytes(batch->total_q);
   a.capacity = hs->capacity;
   a.host_rows = hs->host_rows;
   a.row_elems = hs->row_elems;

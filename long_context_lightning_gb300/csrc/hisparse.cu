@@ -14,35 +14,44 @@
 // slots, the step at which each slot was last used, per-row first-request
 // stamps, this step's misses and their slots, and counters.
 //
-// One fetch = four launches after the per-call plan:
+// One fetch = six launches after the per-call plan, each over many blocks
+// except the scan:
 //   lookup   every selected entry: stamp its host row with (step, entry index)
 //            so the first request of a row is known, and mark resident rows'
 //            slots used in this step
-//   plan     one block: the misses in first-request order; the LRU order
+//   count    per chunk of 2048 entries: first-request misses and hits; per
+//            chunk of 2048 LRU positions: slots not used in this step
+//   scan     one block: chunk offsets, totals, the capacity check
+//   scatter  misses to their place in first-request order; the LRU order
 //            split into [not used this step] ++ [used this step] (stable); the
-//            first misses-many slots of the first part are the victims; new
-//            order = [rest of the first part] ++ [used] ++ [victims]; tables
-//            updated, evicted rows dropped
-//   copy     one warp per miss: the host row into its slot (16-byte loads of
-//            pinned host memory)
+//            first misses-many slots of the first part are the victims (their
+//            rows dropped); new order = [rest of the first part] ++ [used] ++
+//            [victims], written to the other of two order buffers
+//   copy     one warp per miss: bind the victim slot to the row and copy the
+//            host row into it (16-byte loads of pinned host memory)
 //   resolve  every selected entry: the slot now holding its row
 #include "internal.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kPlanThreads = 1024;
-constexpr int kEntryThreads = 256;
+constexpr int kThreads = 256;
+constexpr int kPer = 8;                     // items per thread in the count and scatter passes
+constexpr int kChunk = kThreads * kPer;     // items per block there
+constexpr int kScanThreads = 1024;
 constexpr int kCopyWarps = 8;
 
-enum { ST_STEP = 0, ST_REQUESTS = 1, ST_HITS = 2, ST_MISSES = 3, ST_EVICTED = 4, ST_OVERFLOW = 5 };
+enum {
+  ST_STEP = 0, ST_REQUESTS = 1, ST_HITS = 2, ST_MISSES = 3, ST_EVICTED = 4, ST_OVERFLOW = 5,
+  ST_PARITY = 6,   // which of the two order buffers is current
+  ST_NOT_USED = 7  // slots not used in this step (this fetch's scan)
+};
 
 struct HsState {
   int32_t* slot_of_row;  // [host_rows]
   uint64_t* claim;       // [host_rows]
   int32_t* row_of_slot;  // [capacity]
-  int32_t* lru;          // [capacity] slots, least recently used first
-  int32_t* lru_next;     // [capacity]
+  int32_t* lru[2];       // [capacity] each: slots, least recently used first; stats[ST_PARITY] picks the current
   int32_t* used;         // [capacity] step of the slot's last use
   int32_t* miss_rows;    // [capacity]
   int32_t* miss_slots;   // [capacity]
@@ -61,7 +70,7 @@ HsState carve(void* base, int64_t capacity, int64_t host_rows) {
   p += align_up(4 * (size_t)host_rows, 256);
   s.claim = reinterpret_cast<uint64_t*>(p);
   p += align_up(8 * (size_t)host_rows, 256);
-  int32_t** arr[6] = {&s.row_of_slot, &s.lru, &s.lru_next, &s.used, &s.miss_rows, &s.miss_slots};
+  int32_t** arr[6] = {&s.row_of_slot, &s.lru[0], &s.lru[1], &s.used, &s.miss_rows, &s.miss_slots};
   for (int i = 0; i < 6; ++i) {
     *arr[i] = reinterpret_cast<int32_t*>(p);
     p += align_up(4 * (size_t)capacity, 256);
@@ -70,8 +79,36 @@ HsState carve(void* base, int64_t capacity, int64_t host_rows) {
   return s;
 }
 
+// Per-call chunk counts, carved from the caller's workspace after the plan.
+struct Counts {
+  int32_t* miss;  // [n_entry_chunks] misses per entry chunk, then (after the scan) their offsets
+  int32_t* hit;   // [n_entry_chunks]
+  int32_t* a;     // [n_lru_chunks] not-used slots per LRU chunk, then their offsets
+};
+
+int64_t entry_chunks(int64_t entries) { return (entries + kChunk - 1) / kChunk; }
+int64_t lru_chunks(int64_t capacity) { return (capacity + kChunk - 1) / kChunk; }
+
+size_t counts_bytes(int64_t entries, int64_t capacity) {
+  return 2 * align_up(4 * (size_t)entry_chunks(entries), 256) + align_up(4 * (size_t)lru_chunks(capacity), 256);
+}
+
+Counts carve_counts(void* base, int64_t entries, int64_t capacity) {
+  char* p = static_cast<char*>(base);
+  Counts c;
+  c.miss = reinterpret_cast<int32_t*>(p);
+  p += align_up(4 * (size_t)entry_chunks(entries), 256);
+  c.hit = reinterpret_cast<int32_t*>(p);
+  p += align_up(4 * (size_t)entry_chunks(entries), 256);
+  c.a = reinterpret_cast<int32_t*>(p);
+  return c;
+}
+
 struct HsParams {
   HsState s;
+  Counts c;
+  int32_t n_entry_chunks;
+  int32_t n_lru_chunks;
   int32_t capacity;
   int64_t host_rows;
   int32_t row_elems;
@@ -114,31 +151,13 @@ __device__ __forceinline__ int64_t entry_row(const HsParams& p, int f, bool flag
   return row;
 }
 
-__global__ void hs_reset_kernel(HsState s, int32_t capacity, int64_t host_rows) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < host_rows; i += stride) {
-    s.slot_of_row[i] = -1;
-    s.claim[i] = 0;
-  }
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < capacity; i += stride) {
-    s.row_of_slot[i] = -1;
-    s.lru[i] = (int32_t)i;
-    s.used[i] = 0;  // steps start at 1
-  }
-  if (blockIdx.x == 0 && threadIdx.x < 8) s.stats[threadIdx.x] = 0;
-}
-
-__global__ void __launch_bounds__(kEntryThreads) hs_lookup_kernel(HsParams p) {
-  pdl_wait();  // the plan and the previous fetch are complete from here on
-  pdl_trigger();
-  const int f = blockIdx.x * kEntryThreads + threadIdx.x;
-  if (f >= p.T * p.k) return;
-  const uint32_t step = (uint32_t)p.s.stats[ST_STEP] + 1u;
-  const int64_t row = entry_row(p, f, true);
-  if (row < 0) return;
-  atomicMax(reinterpret_cast<unsigned long long*>(p.s.claim + row), (unsigned long long)claim_key(step, (uint32_t)f));
-  const int slot = p.s.slot_of_row[row];
-  if (slot >= 0) p.s.used[slot] = (int32_t)step;
+// Entry f's status in this step: 1 = first request of a missing row, 2 =
+// first request of a resident row, 0 = anything else.
+__device__ __forceinline__ int entry_kind(const HsParams& p, int f, uint32_t step, int64_t* row_out) {
+  const int64_t row = entry_row(p, f, false);
+  *row_out = row;
+  if (row < 0 || p.s.claim[row] != claim_key(step, (uint32_t)f)) return 0;
+  return p.s.slot_of_row[row] < 0 ? 1 : 2;
 }
 
 // Exclusive block-wide scan of one int per thread (all threads call it).
@@ -168,126 +187,225 @@ __device__ int scan_block(int v, int* warp_sums, int* total) {
   return before;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1) hs_plan_kernel(HsParams p) {
+__global__ void hs_reset_kernel(HsState s, int32_t capacity, int64_t host_rows) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < host_rows; i += stride) {
+    s.slot_of_row[i] = -1;
+    s.claim[i] = 0;
+  }
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < capacity; i += stride) {
+    s.row_of_slot[i] = -1;
+    s.lru[0][i] = (int32_t)i;
+    s.used[i] = 0;  // steps start at 1
+  }
+  if (blockIdx.x == 0 && threadIdx.x < 8) s.stats[threadIdx.x] = 0;
+}
+
+__global__ void __launch_bounds__(kThreads) hs_lookup_kernel(HsParams p) {
+  pdl_wait();  // the plan and the previous fetch are complete from here on
+  pdl_trigger();
+  const int f = blockIdx.x * kThreads + threadIdx.x;
+  if (f >= p.T * p.k) return;
+  const uint32_t step = (uint32_t)p.s.stats[ST_STEP] + 1u;
+  const int64_t row = entry_row(p, f, true);
+  if (row < 0) return;
+  atomicMax(reinterpret_cast<unsigned long long*>(p.s.claim + row), (unsigned long long)claim_key(step, (uint32_t)f));
+  const int slot = p.s.slot_of_row[row];
+  if (slot >= 0) p.s.used[slot] = (int32_t)step;
+}
+
+__global__ void __launch_bounds__(kThreads) hs_count_kernel(HsParams p) {
   __shared__ int warp_sums[32];
-  __shared__ int s_overflow;
   pdl_wait();
   pdl_trigger();
-  const int tid = threadIdx.x;
   const uint32_t step = (uint32_t)p.s.stats[ST_STEP] + 1u;
-  const int cap = p.capacity;
-
-  // (1) distinct requested rows in first-request order: misses compacted, hits counted
-  int n_miss = 0, n_hit = 0;
   const int n_entries = p.T * p.k;
-  for (int f0 = 0; f0 < n_entries; f0 += kPlanThreads) {
-    const int f = f0 + tid;
+  if ((int)blockIdx.x < p.n_entry_chunks) {
     int miss = 0, hit = 0;
-    int64_t row = -1;
-    if (f < n_entries) {
-      row = entry_row(p, f, false);
-      if (row >= 0 && p.s.claim[row] == claim_key(step, (uint32_t)f)) {
-        miss = p.s.slot_of_row[row] < 0;
-        hit = !miss;
-      }
+    const int f0 = blockIdx.x * kChunk + threadIdx.x * kPer;
+    for (int i = 0; i < kPer; ++i) {
+      if (f0 + i >= n_entries) break;
+      int64_t row;
+      const int kind = entry_kind(p, f0 + i, step, &row);
+      miss += kind == 1;
+      hit += kind == 2;
     }
     int tot_m, tot_h;
-    const int ex = scan_block(miss, warp_sums, &tot_m);
+    scan_block(miss, warp_sums, &tot_m);
     scan_block(hit, warp_sums, &tot_h);
-    if (miss && n_miss + ex < cap) p.s.miss_rows[n_miss + ex] = (int32_t)row;
-    n_miss += tot_m;
-    n_hit += tot_h;
-  }
-  // every requested row must fit: the slots used this step (n_hit) plus the misses
-  if (tid == 0) s_overflow = (n_miss > cap - n_hit) ? 1 : 0;
-  __syncthreads();
-  if (s_overflow) {
-    if (tid == 0) {
-      atomicOr(p.err, DEV_ERR_CAPACITY);
-      p.s.stats[ST_OVERFLOW] = 1;
-      p.s.stats[ST_MISSES] = 0;
-      p.s.stats[ST_STEP] = (int32_t)step;
+    if (threadIdx.x == 0) {
+      p.c.miss[blockIdx.x] = tot_m;
+      p.c.hit[blockIdx.x] = tot_h;
     }
-    return;
-  }
-
-  // (2) LRU order: [not used this step] ++ [used this step], both stable; the
-  // first n_miss of the first part are the victims and go to the end
-  int n_a = 0;
-  for (int i0 = 0; i0 < cap; i0 += kPlanThreads) {
-    const int i = i0 + tid;
-    const int a = (i < cap && p.s.used[p.s.lru[i]] != (int32_t)step) ? 1 : 0;
+  } else {
+    const int chunk = blockIdx.x - p.n_entry_chunks;
+    const int32_t* lru = p.s.lru[p.s.stats[ST_PARITY] & 1];
+    int a = 0;
+    const int i0 = chunk * kChunk + threadIdx.x * kPer;
+    for (int i = 0; i < kPer; ++i) {
+      if (i0 + i >= p.capacity) break;
+      const int slot = lru[i0 + i];
+      if ((unsigned)slot >= (unsigned)p.capacity) {  // the order is a permutation of the slots
+        atomicOr(p.err, DEV_ERR_BAD_INDEX);
+        continue;
+      }
+      a += p.s.used[slot] != (int32_t)step;
+    }
     int tot;
     scan_block(a, warp_sums, &tot);
-    n_a += tot;
+    if (threadIdx.x == 0) p.c.a[chunk] = tot;
   }
-  int a_run = 0, b_run = 0, evicted = 0;
-  for (int i0 = 0; i0 < cap; i0 += kPlanThreads) {
-    const int i = i0 + tid;
-    int slot = -1, is_a = 0, is_b = 0;
-    if (i < cap) {
-      slot = p.s.lru[i];
-      is_a = p.s.used[slot] != (int32_t)step;
-      is_b = !is_a;
+}
+
+// In-place exclusive scan of n ints by one block; returns the total.
+__device__ int scan_array(int32_t* v, int n, int* warp_sums) {
+  int running = 0;
+  for (int i0 = 0; i0 < n; i0 += kScanThreads) {
+    const int i = i0 + threadIdx.x;
+    const int x = i < n ? v[i] : 0;
+    int tot;
+    const int ex = scan_block(x, warp_sums, &tot);
+    if (i < n) v[i] = running + ex;
+    running += tot;
+  }
+  return running;
+}
+
+__global__ void __launch_bounds__(kScanThreads, 1) hs_scan_kernel(HsParams p) {
+  __shared__ int warp_sums[32];
+  pdl_wait();
+  pdl_trigger();
+  const int n_miss = scan_array(p.c.miss, p.n_entry_chunks, warp_sums);
+  int n_hit = 0;
+  for (int i = threadIdx.x; i < p.n_entry_chunks; i += kScanThreads) n_hit += p.c.hit[i];
+  int tot_h;
+  scan_block(n_hit, warp_sums, &tot_h);
+  const int n_a = scan_array(p.c.a, p.n_lru_chunks, warp_sums);
+  if (threadIdx.x == 0) {
+    // every requested row must fit: each miss takes a slot not used in this step
+    const int overflow = n_miss > n_a;
+    p.s.stats[ST_NOT_USED] = n_a;
+    if (overflow) atomicOr(p.err, DEV_ERR_CAPACITY);
+    p.s.stats[ST_OVERFLOW] = overflow;
+    p.s.stats[ST_REQUESTS] = tot_h + n_miss;
+    p.s.stats[ST_HITS] = tot_h;
+    p.s.stats[ST_MISSES] = overflow ? 0 : n_miss;
+    p.s.stats[ST_EVICTED] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) hs_scatter_kernel(HsParams p) {
+  __shared__ int warp_sums[32];
+  pdl_wait();
+  pdl_trigger();
+  if (p.s.stats[ST_OVERFLOW]) return;
+  const uint32_t step = (uint32_t)p.s.stats[ST_STEP] + 1u;
+  const int n_miss = p.s.stats[ST_MISSES];
+  const int cap = p.capacity;
+  const int n_entries = p.T * p.k;
+  if ((int)blockIdx.x < p.n_entry_chunks) {
+    // misses in first-request (flat entry) order
+    int kinds[kPer];
+    int64_t rows[kPer];
+    int miss = 0;
+    const int f0 = blockIdx.x * kChunk + threadIdx.x * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      kinds[i] = 0;
+      rows[i] = -1;
+      if (f0 + i < n_entries) kinds[i] = entry_kind(p, f0 + i, step, &rows[i]);
+      miss += kinds[i] == 1;
     }
-    int tot_a, tot_b, tot_e;
-    const int ea = scan_block(is_a, warp_sums, &tot_a);
-    const int eb = scan_block(is_b, warp_sums, &tot_b);
-    int ev = 0;
-    if (is_a) {
-      const int a = a_run + ea;
-      if (a < n_miss) {
-        // victim a receives miss row a; its old row (if any) leaves HBM
-        const int old = p.s.row_of_slot[slot];
-        if (old >= 0) {
-          p.s.slot_of_row[old] = -1;
-          ev = 1;
+    int tot;
+    int pos = p.c.miss[blockIdx.x] + scan_block(miss, warp_sums, &tot);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if (kinds[i] == 1) p.s.miss_rows[pos++] = (int32_t)rows[i];
+  } else {
+    const int chunk = blockIdx.x - p.n_entry_chunks;
+    const int par = p.s.stats[ST_PARITY] & 1;
+    const int32_t* lru = p.s.lru[par];
+    int32_t* nxt = p.s.lru[par ^ 1];
+    const int n_a = p.s.stats[ST_NOT_USED];
+    int slots[kPer], is_a[kPer];
+    int a = 0;
+    const int i0 = chunk * kChunk + threadIdx.x * kPer;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      slots[i] = -1;
+      is_a[i] = 0;
+      if (i0 + i < cap) {
+        const int slot = lru[i0 + i];
+        if ((unsigned)slot < (unsigned)cap) {
+          slots[i] = slot;
+          is_a[i] = p.s.used[slot] != (int32_t)step;
         }
-        const int row = p.s.miss_rows[a];
-        p.s.row_of_slot[slot] = row;
-        p.s.slot_of_row[row] = slot;
-        p.s.used[slot] = (int32_t)step;
-        p.s.miss_slots[a] = slot;
-        p.s.lru_next[cap - n_miss + a] = slot;
-      } else {
-        p.s.lru_next[a - n_miss] = slot;
       }
-    } else if (is_b) {
-      p.s.lru_next[n_a - n_miss + b_run + eb] = slot;
+      a += is_a[i];
     }
-    scan_block(ev, warp_sums, &tot_e);
-    a_run += tot_a;
-    b_run += tot_b;
-    evicted += tot_e;
-  }
-  __syncthreads();
-  for (int i = tid; i < cap; i += kPlanThreads) p.s.lru[i] = p.s.lru_next[i];
-  if (tid == 0) {
-    p.s.stats[ST_REQUESTS] = n_hit + n_miss;
-    p.s.stats[ST_HITS] = n_hit;
-    p.s.stats[ST_MISSES] = n_miss;
-    p.s.stats[ST_EVICTED] = evicted;
-    p.s.stats[ST_OVERFLOW] = 0;
-    p.s.stats[ST_STEP] = (int32_t)step;
+    int tot;
+    // order: [not-used, not victims] ++ [used] ++ [victims]; a_idx / b_idx count
+    // the not-used / used slots before this thread's first one
+    int a_idx = p.c.a[chunk] + scan_block(a, warp_sums, &tot);
+    int b_idx = i0 - a_idx;
+    int evicted = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      if (slots[i] < 0) continue;
+      const int slot = slots[i];
+      if (is_a[i]) {
+        if (a_idx < n_miss) {
+          // victim a_idx receives miss row a_idx (bound in the copy pass); its old row leaves HBM
+          const int old = p.s.row_of_slot[slot];
+          if (old >= 0) {
+            p.s.slot_of_row[old] = -1;
+            ++evicted;
+          }
+          p.s.miss_slots[a_idx] = slot;
+          nxt[cap - n_miss + a_idx] = slot;
+        } else {
+          nxt[a_idx - n_miss] = slot;
+        }
+        ++a_idx;
+      } else {
+        nxt[n_a - n_miss + b_idx] = slot;
+        ++b_idx;
+      }
+    }
+    int tot_e;
+    scan_block(evicted, warp_sums, &tot_e);
+    if (threadIdx.x == 0 && tot_e) atomicAdd(p.s.stats + ST_EVICTED, tot_e);
   }
 }
 
 __global__ void __launch_bounds__(32 * kCopyWarps) hs_copy_kernel(HsParams p) {
   pdl_wait();
   pdl_trigger();
+  const uint32_t step = (uint32_t)p.s.stats[ST_STEP] + 1u;
+  const bool overflow = p.s.stats[ST_OVERFLOW] != 0;
   const int a = blockIdx.x * kCopyWarps + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (a >= p.s.stats[ST_MISSES]) return;
-  const int64_t row = p.s.miss_rows[a];
-  const int64_t slot = p.s.miss_slots[a];
-  const uint4* src = reinterpret_cast<const uint4*>(p.host.base + row * p.host.row_stride);
-  uint4* dst = reinterpret_cast<uint4*>(p.slot_pool + slot * p.slot_stride);
+  if (overflow || a >= p.s.stats[ST_MISSES]) return;
+  const int row = p.s.miss_rows[a];
+  const int slot = p.s.miss_slots[a];
+  if (lane == 0) {
+    p.s.row_of_slot[slot] = row;
+    p.s.slot_of_row[row] = slot;
+    p.s.used[slot] = (int32_t)step;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(p.host.base + (int64_t)row * p.host.row_stride);
+  uint4* dst = reinterpret_cast<uint4*>(p.slot_pool + (int64_t)slot * p.slot_stride);
   for (int i = lane; i < p.row_elems / 8; i += 32) dst[i] = src[i];
 }
 
-__global__ void __launch_bounds__(kEntryThreads) hs_resolve_kernel(HsParams p) {
+__global__ void __launch_bounds__(kThreads) hs_resolve_kernel(HsParams p) {
   pdl_wait();
   pdl_trigger();
-  const int f = blockIdx.x * kEntryThreads + threadIdx.x;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // the step is over: nothing after this kernel in the fetch reads the step or the parity
+    p.s.stats[ST_STEP] += 1;
+    if (!p.s.stats[ST_OVERFLOW]) p.s.stats[ST_PARITY] ^= 1;
+  }
+  const int f = blockIdx.x * kThreads + threadIdx.x;
   if (f >= p.T * p.k) return;
   const int t = f / p.k, j = f - t * p.k;
   const int64_t row = entry_row(p, f, false);
@@ -295,8 +413,11 @@ __global__ void __launch_bounds__(kEntryThreads) hs_resolve_kernel(HsParams p) {
 }
 
 __global__ void hs_resident_kernel(HsState s, int32_t capacity, int32_t* rows) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < capacity; i += gridDim.x * blockDim.x)
-    rows[i] = s.row_of_slot[s.lru[i]];
+  const int32_t* lru = s.lru[s.stats[ST_PARITY] & 1];
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < capacity; i += gridDim.x * blockDim.x) {
+    const int slot = lru[i];
+    rows[i] = (unsigned)slot < (unsigned)capacity ? s.row_of_slot[slot] : -1;
+  }
 }
 
 cudaError_t launch_pdl(const void* kern, int grid, int block, void** args, cudaStream_t stream) {
@@ -314,6 +435,8 @@ cudaError_t launch_pdl(const void* kern, int grid, int block, void** args, cudaS
 
 size_t hisparse_state_bytes(int64_t capacity, int64_t host_rows) { return state_bytes(capacity, host_rows); }
 
+size_t hisparse_counts_bytes(int64_t entries, int64_t capacity) { return counts_bytes(entries, capacity); }
+
 cudaError_t launch_hisparse_reset(void* state, int32_t capacity, int64_t host_rows, cudaStream_t stream) {
   const HsState s = carve(state, capacity, host_rows);
   const int64_t n = std::max<int64_t>(host_rows, capacity);
@@ -323,8 +446,12 @@ cudaError_t launch_hisparse_reset(void* state, int32_t capacity, int64_t host_ro
 }
 
 cudaError_t launch_hisparse_fetch(const HisparseLaunch& a, cudaStream_t stream) {
+  const int64_t n = (int64_t)a.T * a.k;
   HsParams p;
   p.s = carve(a.state, a.capacity, a.host_rows);
+  p.c = carve_counts(a.counts, n, a.capacity);
+  p.n_entry_chunks = (int32_t)entry_chunks(n);
+  p.n_lru_chunks = (int32_t)lru_chunks(a.capacity);
   p.capacity = a.capacity;
   p.host_rows = a.host_rows;
   p.row_elems = a.row_elems;
@@ -341,17 +468,19 @@ cudaError_t launch_hisparse_fetch(const HisparseLaunch& a, cudaStream_t stream) 
   p.ld_slots = a.ld_slots;
   p.err = a.err;
   void* args[] = {&p};
-  const int n = a.T * a.k;
-  const int entry_grid = (n + kEntryThreads - 1) / kEntryThreads;
+  const int entry_grid = (int)((n + kThreads - 1) / kThreads);
+  const int chunk_grid = p.n_entry_chunks + p.n_lru_chunks;
+  const int max_miss = (int)std::min<int64_t>(n, a.capacity);
+  const int copy_grid = std::max(1, (max_miss + kCopyWarps - 1) / kCopyWarps);
   cudaError_t e;
-  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_lookup_kernel), entry_grid, kEntryThreads, args, stream)))
+  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_lookup_kernel), entry_grid, kThreads, args, stream))) return e;
+  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_count_kernel), chunk_grid, kThreads, args, stream))) return e;
+  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_scan_kernel), 1, kScanThreads, args, stream))) return e;
+  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_scatter_kernel), chunk_grid, kThreads, args, stream)))
     return e;
-  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_plan_kernel), 1, kPlanThreads, args, stream))) return e;
-  const int max_miss = std::min(n, a.capacity);
-  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_copy_kernel), std::max(1, (max_miss + kCopyWarps - 1) / kCopyWarps),
-                      32 * kCopyWarps, args, stream)))
+  if ((e = launch_pdl(reinterpret_cast<const void*>(hs_copy_kernel), copy_grid, 32 * kCopyWarps, args, stream)))
     return e;
-  return launch_pdl(reinterpret_cast<const void*>(hs_resolve_kernel), entry_grid, kEntryThreads, args, stream);
+  return launch_pdl(reinterpret_cast<const void*>(hs_resolve_kernel), entry_grid, kThreads, args, stream);
 }
 
 cudaError_t launch_hisparse_resident(void* state, int32_t capacity, int64_t host_rows, int32_t* rows,

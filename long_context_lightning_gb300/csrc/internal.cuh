@@ -173,6 +173,7 @@ cudaError_t launch_cache_append(const AppendLaunch& a, cudaStream_t stream);
 
 struct HisparseLaunch {
   void* state;
+  void* counts;  // hisparse_counts_bytes(T * k, capacity) bytes of the caller's workspace
   int32_t capacity;
   int64_t host_rows;
   int32_t row_elems;
@@ -190,6 +191,7 @@ struct HisparseLaunch {
   int* err;
 };
 size_t hisparse_state_bytes(int64_t capacity, int64_t host_rows);
+size_t hisparse_counts_bytes(int64_t entries, int64_t capacity);
 cudaError_t launch_hisparse_reset(void* state, int32_t capacity, int64_t host_rows, cudaStream_t stream);
 cudaError_t launch_hisparse_fetch(const HisparseLaunch& a, cudaStream_t stream);
 cudaError_t launch_hisparse_resident(void* state, int32_t capacity, int64_t host_rows, int32_t* rows,

@@ -91,7 +91,7 @@ def test_lru_steps_match_oracle(lib, name, kw, slack):
     total_evicted = 0
     for step, idx in enumerate(sels, start=1):
         idx_d = idx.cuda()
-        hc.fetch(sa.batch, idx_d, k, slots, sa.workspace)
+        hc.fetch(sa.batch, idx_d, k, slots)
         assert lib.check_device_error() == lib.DSA_OK
         hits, misses, evicted = lru.step(_oracle_rows(wl_cpu, idx))
         total_evicted += len(evicted)
@@ -128,7 +128,7 @@ def test_attention_over_slots_matches_oracle(lib):
     out = torch.empty_like(sa.outs[0])
     lse = torch.empty_like(sa.lses[0])
     idx = _selection(wl, 3, k)
-    hc.fetch(sa.batch, idx.cuda(), k, slots, sa.workspace)
+    hc.fetch(sa.batch, idx.cuda(), k, slots)
     lib.sparse_mla_fwd(sa.batch, hc.layer(wl.q[0], spec.d_v, spec.scale), slots, k, out, lse, sa.workspace)
     torch.cuda.synchronize()
     assert lib.check_device_error() == lib.DSA_OK
@@ -149,14 +149,14 @@ def test_capacity_overflow_changes_nothing(lib):
     slots = torch.empty((T, k), dtype=torch.int32, device="cuda")
     first = _selection(wl, 2, k)
     first[1:] = -1                                   # one query: 2048 - a few rows, fits
-    hc.fetch(sa.batch, first.cuda(), k, slots, sa.workspace)
+    hc.fetch(sa.batch, first.cuda(), k, slots)
     assert lib.check_device_error() == lib.DSA_OK
     before = hc.resident()
     want = _oracle_rows(wl_cpu, _selection(wl, 5, k))
     assert len(want) > 5000
     over = _selection(wl, 5, k)
     over[0, :k] = first[0, :k]                       # query 0's rows are all resident (hits)
-    hc.fetch(sa.batch, over.cuda(), k, slots, sa.workspace)
+    hc.fetch(sa.batch, over.cuda(), k, slots)
     assert lib.check_device_error() == lib.DSA_ERR_CAPACITY
     assert hc.resident() == before
     st = hc.stats()
@@ -170,7 +170,7 @@ def test_capacity_overflow_changes_nothing(lib):
     lru.step(_oracle_rows(wl_cpu, first))
     nxt = _selection(wl, 7, k)
     nxt[2:] = -1
-    hc.fetch(sa.batch, nxt.cuda(), k, slots, sa.workspace)
+    hc.fetch(sa.batch, nxt.cuda(), k, slots)
     assert lib.check_device_error() == lib.DSA_OK
     hits, misses, evicted = lru.step(_oracle_rows(wl_cpu, nxt))
     assert hc.resident() == list(lru.order)
