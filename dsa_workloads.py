@@ -23,6 +23,13 @@ Shapes and distributions follow the five workloads the library is measured on:
               tokens (32768 entries), top-512 entries; indexer 64 x 128,
               64-head MQA over 576-dim entries.
   csa_pro     as csa_flash with top-1024 entries.
+  mha         MHA mode ("How GLM5.3 ...", Model: vLLM switches to MHA mode for
+              about 2K-5K tokens): 1 sequence, context 4608, the last 3072
+              positions are queries (the first 512 of them see at most 2048
+              tokens: dense); indexer 64 x 128, top-k 2048; 64 heads whose
+              keys (192 no-rope dims up-projected from the 512-dim latent, plus
+              the 64 shared rope dims) and values (256 dims up-projected) come
+              from the 576-dim latent rows; per-head queries of 256 dims.
 
 The model shapes come from "How GLM5.3 Sparse Attention Affects HBM Memory
 Usage" (How it works / Model: 64 query heads, top-k 2048, dense below 2K;
@@ -34,7 +41,9 @@ Recipe (device independent up to the device's own generator):
   * every tensor has its own generator, torch.Generator(device).manual_seed(
     seed * 1000 + tensor_id); tensor ids: 0 lengths, 1 page permutation,
     2 indexer queries, 3 head weights, 4 indexer keys, 10+l layer-l queries,
-    20+l layer-l latent cache.  Any tensor can thus be redrawn alone.
+    20+l layer-l latent cache, 30+l layer-l MHA queries, 40+l layer-l key
+    up-projection, 50+l layer-l value up-projection.  Any tensor can thus be
+    redrawn alone.
   * normal draws are float32 torch.randn scaled by the stated std, then rounded
     to bfloat16 (round to nearest even); integer draws are torch.randint.
   * queries of sequence b are its LAST q_per_seq positions.
@@ -49,6 +58,7 @@ import torch
 
 # tensor ids for per-tensor generators
 _T_LENS, _T_PAGES, _T_QIDX, _T_W, _T_KIDX, _T_Q, _T_KV = 0, 1, 2, 3, 4, 10, 20
+_T_QMHA, _T_WUK, _T_WUV = 30, 40, 50
 
 
 @dataclasses.dataclass(frozen=True)
@@ -71,6 +81,10 @@ class Spec:
     page_size: int = 64
     integer_indexer: bool = False
     compress_ratio: int = 1         # tokens per cache entry (1: one entry per token)
+    mha: bool = False               # MHA mode: per-head keys/values up-projected from the latent
+    d_nope: int = 192               # MHA: up-projected no-rope key dims per head (rope = d_qk - d_v)
+    d_vh: int = 256                 # MHA: up-projected value dims per head
+    q_mha_std: float = 1.0
     idx_std: float = 1.0 / math.sqrt(128.0)
     w_std: float = 1.0 / 8.0
     kv_std: float = 0.05
@@ -102,6 +116,9 @@ SPECS = {
     "csa_pro": Spec(name="csa_pro", seed=6, batch=32, ctx_len=131072, ctx_range=None, q_per_seq=1,
                     idx_heads=64, idx_dim=128, topk=1024, heads=64, d_qk=576, d_v=512,
                     scale=1.0 / 16.0, compress_ratio=4),
+    "mha": Spec(name="mha", seed=7, batch=1, ctx_len=4608, ctx_range=None, q_per_seq=3072,
+                idx_heads=64, idx_dim=128, topk=2048, heads=64, d_qk=576, d_v=512,
+                scale=1.0 / 16.0, mha=True),
 }
 
 
@@ -135,6 +152,9 @@ class Workload:
     kv: List[torch.Tensor]
     seq_start: Optional[torch.Tensor] = None
     page_table: Optional[torch.Tensor] = None
+    q_mha: Optional[List[torch.Tensor]] = None   # MHA mode: per layer bf16 [T, H, d_nope + rope]
+    w_uk: Optional[List[torch.Tensor]] = None    # per layer bf16 [H, d_nope, d_v]
+    w_uv: Optional[List[torch.Tensor]] = None    # per layer bf16 [H, d_vh, d_v]
 
     @property
     def total_q(self) -> int:
@@ -162,7 +182,10 @@ class Workload:
             self, seq_lens=mv(self.seq_lens), cu_seqlens_q=mv(self.cu_seqlens_q),
             q_idx=mv(self.q_idx), w=mv(self.w), k_idx=mv(self.k_idx),
             q=[mv(t) for t in self.q], kv=[mv(t) for t in self.kv] if kv_too else self.kv,
-            seq_start=mv(self.seq_start), page_table=mv(self.page_table))
+            seq_start=mv(self.seq_start), page_table=mv(self.page_table),
+            q_mha=None if self.q_mha is None else [mv(t) for t in self.q_mha],
+            w_uk=None if self.w_uk is None else [mv(t) for t in self.w_uk],
+            w_uv=None if self.w_uv is None else [mv(t) for t in self.w_uv])
 
 
 def _gen(spec: Spec, tensor_id: int, device) -> torch.Generator:
@@ -235,10 +258,24 @@ def make_workload(spec: Spec, device="cpu", kv_device=None) -> Workload:
         q.append(_normal_bf16((T, spec.heads, spec.d_qk), spec.kv_std, _gen(spec, _T_Q + layer, device), device))
         kv.append(_normal_bf16((rows, spec.d_qk), spec.kv_std, _gen(spec, _T_KV + layer, kv_device), kv_device))
 
+    q_mha = w_uk = w_uv = None
+    if spec.mha:
+        rope = spec.d_qk - spec.d_v
+        q_mha, w_uk, w_uv = [], [], []
+        for layer in range(spec.n_layers):
+            q_mha.append(_normal_bf16((T, spec.heads, spec.d_nope + rope), spec.q_mha_std,
+                                      _gen(spec, _T_QMHA + layer, device), device))
+            # unit-gain up-projections: a projected row keeps the latent's scale
+            w_uk.append(_normal_bf16((spec.heads, spec.d_nope, spec.d_v), 1.0 / math.sqrt(spec.d_v),
+                                     _gen(spec, _T_WUK + layer, device), device))
+            w_uv.append(_normal_bf16((spec.heads, spec.d_vh, spec.d_v), 1.0 / math.sqrt(spec.d_v),
+                                     _gen(spec, _T_WUV + layer, device), device))
+
     return Workload(spec=spec, seq_lens=lens.to(device), cu_seqlens_q=cu.to(device), q_idx=q_idx, w=w,
                     k_idx=k_idx, q=q, kv=kv,
                     seq_start=None if seq_start is None else seq_start.to(device),
-                    page_table=None if page_table is None else page_table.to(device))
+                    page_table=None if page_table is None else page_table.to(device),
+                    q_mha=q_mha, w_uk=w_uk, w_uv=w_uv)
 
 
 def pool_rows(wl: Workload, b: int, positions: torch.Tensor) -> torch.Tensor:

@@ -40,6 +40,12 @@ What is computed, and where it is defined:
                       m - 1 and is visible to a query at position p once its
                       block is complete, so the query sees floor((p + 1) / m)
                       entries.
+  MHA mode            the same selection; each head's key is the head's
+                      up-projection of the latent's first D_v dims followed by
+                      the shared rope dims, its value the head's value
+                      up-projection; softmax attention per head with the head's
+                      own query ("How GLM5.3 ...", Model, second bullet: vLLM
+                      switches sparse MLA to MHA mode for about 2K-5K tokens).
 
 Readings where the pages are silent:
   * one indexer key per token, shared by all indexer heads;
@@ -119,6 +125,55 @@ def sparse_mla(q: np.ndarray, rows: np.ndarray, scale: float, d_v: int):
 # ---------------------------------------------------------------------------
 # whole forward over a workload
 # ---------------------------------------------------------------------------
+
+def mha_upproject(c_rows: np.ndarray, w_uk: np.ndarray, w_uv: np.ndarray):
+    """Per-head keys and values of MHA mode from latent rows.
+
+    c_rows [m, D]: the first L dims are the compressed latent, the other D - L
+    the rope key every head shares; w_uk [H, d_nope, L]; w_uv [H, d_vh, L].
+    Returns K [m, H, d_nope + D - L] with K[s, h] = (w_uk[h] @ c[s, :L], c[s, L:])
+    and V [m, H, d_vh] with V[s, h] = w_uv[h] @ c[s, :L].
+    """
+    L = w_uk.shape[2]
+    m, H = c_rows.shape[0], w_uk.shape[0]
+    lat = c_rows[:, :L]
+    k_nope = np.stack([lat @ w_uk[h].T for h in range(H)], axis=1)      # [m, H, d_nope]
+    rope = np.broadcast_to(c_rows[:, None, L:], (m, H, c_rows.shape[1] - L))
+    v = np.stack([lat @ w_uv[h].T for h in range(H)], axis=1)           # [m, H, d_vh]
+    return np.concatenate([k_nope, rope], axis=2), v
+
+
+def sparse_mha(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Softmax attention of every head over its own keys and values of the
+    selected rows: q [H, d_qk], K [m, H, d_qk], V [m, H, d_vh] -> O [H, d_vh],
+    LSE [H].  An empty selection gives O = 0 and LSE = -inf."""
+    H = q.shape[0]
+    if K.shape[0] == 0:
+        return np.zeros((H, V.shape[2])), np.full(H, -np.inf)
+    O = np.zeros((H, V.shape[2]))
+    lse = np.zeros(H)
+    for h in range(H):
+        z = scale * (K[:, h, :] @ q[h])       # [m]
+        mx = z.max()
+        e = np.exp(z - mx)
+        Z = e.sum()
+        O[h] = (e @ V[:, h, :]) / Z
+        lse[h] = mx + math.log(Z)
+    return O, lse
+
+
+def mha_attention_on_set(wl, t: int, layer: int, sel: np.ndarray):
+    """MHA-mode attention of query t over the index set `sel` (entries < 0
+    skipped): the selected latent rows up-projected per head, then sparse_mha."""
+    seq, pos = _query_table(wl)
+    sel = np.asarray(sel, dtype=np.int64)
+    sel = sel[sel >= 0]
+    rows = _rows_of(wl, seq[t], sel)
+    pool = wl.kv[layer]
+    c = bf16_to_f64(pool[torch.from_numpy(rows).to(pool.device)])
+    K, V = mha_upproject(c, bf16_to_f64(wl.w_uk[layer]), bf16_to_f64(wl.w_uv[layer]))
+    return sparse_mha(bf16_to_f64(wl.q_mha[layer][t]), K, V, wl.spec.scale)
+
 
 def _rows_of(wl, b: int, positions: np.ndarray) -> np.ndarray:
     """Pool rows holding tokens `positions` of sequence b (layout lookup)."""

@@ -478,3 +478,83 @@ def test_lru_invariants_on_random_traces():
                 assert max(last_use[e] for e in evicted) <= min(last_use[k] for k in kept_old)
             for x in want:
                 last_use[x] = s
+
+
+# --------------------------------------------------------------- MHA mode ---
+
+def test_mha_hand_computed_example():
+    # one head, latent L = 2 plus one rope dim, one no-rope key dim, one value dim
+    c = np.array([[1.0, 0.0, 2.0], [0.0, 1.0, -1.0]])
+    w_uk = np.array([[[1.0, 2.0]]])            # k_nope(s) = c0 + 2 c1
+    w_uv = np.array([[[3.0, -1.0]]])           # v(s) = 3 c0 - c1
+    K, V = oracle.mha_upproject(c, w_uk, w_uv)
+    np.testing.assert_array_equal(K[:, 0, :], [[1.0, 2.0], [2.0, -1.0]])
+    np.testing.assert_array_equal(V[:, 0, :], [[3.0], [-1.0]])
+    O, lse = oracle.sparse_mha(np.array([[1.0, 1.0]]), K, V, 1.0)
+    p0 = 1.0 / (1.0 + math.exp(-2.0))          # logits 3 and 1
+    assert abs(O[0, 0] - (4.0 * p0 - 1.0)) < 1e-15
+    assert abs(lse[0] - (3.0 + math.log1p(math.exp(-2.0)))) < 1e-15
+
+
+def test_mha_equals_mqa_with_absorbed_projections():
+    # q_nope . (W_UK c) = (W_UK^T q_nope) . c and sum p (W_UV c) = W_UV sum p c: MHA mode
+    # is the MQA latent attention with the absorbed query, its output up-projected
+    rng = np.random.default_rng(7)
+    H, L, rope, dn, dv, m = 3, 16, 4, 6, 5, 9
+    c = rng.normal(size=(m, L + rope))
+    w_uk = rng.normal(size=(H, dn, L))
+    w_uv = rng.normal(size=(H, dv, L))
+    q = rng.normal(size=(H, dn + rope))
+    scale = 0.3
+    K, V = oracle.mha_upproject(c, w_uk, w_uv)
+    O, lse = oracle.sparse_mha(q, K, V, scale)
+    q_abs = np.stack([np.concatenate([w_uk[h].T @ q[h, :dn], q[h, dn:]]) for h in range(H)])
+    o_lat, lse_lat = oracle.sparse_mla(q_abs, c, scale, L)
+    for h in range(H):
+        np.testing.assert_allclose(O[h], w_uv[h] @ o_lat[h], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_lat, rtol=1e-12, atol=1e-12)
+
+
+def test_mha_dense_case_equals_library_attention():
+    rng = np.random.default_rng(3)
+    H, m, dqk, dv = 4, 13, 8, 6
+    K = rng.normal(size=(m, H, dqk))
+    V = rng.normal(size=(m, H, dv))
+    q = rng.normal(size=(H, dqk))
+    O, lse = oracle.sparse_mha(q, K, V, 0.5)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, None, :], torch.from_numpy(K).permute(1, 0, 2), torch.from_numpy(V).permute(1, 0, 2),
+        scale=0.5)
+    np.testing.assert_allclose(O, ref[:, 0, :].numpy(), rtol=1e-12, atol=1e-12)
+    ref_lse = torch.logsumexp(0.5 * torch.einsum("hd,mhd->hm", torch.from_numpy(q), torch.from_numpy(K)), dim=1)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mha_order_invariant_and_empty_selection():
+    rng = np.random.default_rng(5)
+    K = rng.normal(size=(7, 2, 4))
+    V = rng.normal(size=(7, 2, 3))
+    q = rng.normal(size=(2, 4))
+    perm = rng.permutation(7)
+    a = oracle.sparse_mha(q, K, V, 1.0)
+    b = oracle.sparse_mha(q, K[perm], V[perm], 1.0)
+    np.testing.assert_allclose(a[0], b[0], rtol=1e-13, atol=1e-13)
+    O, lse = oracle.sparse_mha(q, K[:0], V[:0], 1.0)
+    assert (O == 0).all() and np.isneginf(lse).all()
+
+
+def test_mha_workload_reads_the_selected_rows():
+    spec = W.SPECS["mha"].scaled(ctx_len=300, q_per_seq=20, idx_heads=4, idx_dim=32, topk=64, heads=2)
+    wl = W.make_workload(spec)
+    seq, pos = wl.query_positions()
+    t = 5
+    sel = np.array([3, 40, -1, 17], dtype=np.int64)
+    O, lse = oracle.mha_attention_on_set(wl, t, 0, sel)
+    rows = W.pool_rows(wl, seq[t], torch.tensor([3, 40, 17]))
+    c = oracle.bf16_to_f64(wl.kv[0][rows])
+    K, V = oracle.mha_upproject(c, oracle.bf16_to_f64(wl.w_uk[0]), oracle.bf16_to_f64(wl.w_uv[0]))
+    O2, lse2 = oracle.sparse_mha(oracle.bf16_to_f64(wl.q_mha[0][t]), K, V, spec.scale)
+    np.testing.assert_array_equal(O, O2)
+    assert wl.q_mha[0].shape == (20, 2, 256) and wl.w_uk[0].shape == (2, 192, 512)
+    assert wl.w_uv[0].shape == (2, 256, 512)
+    assert pos[0] == 280 and pos[-1] == 299
