@@ -326,6 +326,72 @@ dsa_status_t dsa_hisparse_resident(const dsa_hisparse_t* hs, int32_t* rows, cuda
 dsa_status_t dsa_hisparse_stats(const dsa_hisparse_t* hs, int32_t* stats, cudaStream_t stream);
 
 /*
+ * MHA mode ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it
+ * works / Model: vLLM switches sparse MLA to MHA mode for contexts of about
+ * 2K-5K tokens).  Instead of attending over the 576-dim latent rows with the
+ * up-projections absorbed (MQA mode), every token of a short context is
+ * up-projected once into per-head keys and values, and each head attends with
+ * its own 256-dim query over the same top-k selection.  Shapes are fixed:
+ * latent = 512 compressed dims + 64 rope dims (the latent row of the MQA
+ * path), keys = 192 up-projected dims + the 64 rope dims, values = 256
+ * up-projected dims.
+ */
+#define DSA_MHA_LATENT 512
+#define DSA_MHA_ROPE 64
+#define DSA_MHA_HEAD_DIM 256
+#define DSA_MHA_MAX_HEADS 128
+#define DSA_MHA_MAX_CONTEXT 131072
+
+/*
+ * dsa_mha_project -- per-head keys and values of `rows` latent rows:
+ *   k_out[r, h, 0:192]   = W_UK[h] (192 x 512) . latent[r, 0:512]
+ *   k_out[r, h, 192:256] = latent[r, 512:576]
+ *   v_out[r, h, 0:256]   = W_UV[h] (256 x 512) . latent[r, 0:512]
+ * latent: device bf16 [rows, latent_stride] (latent_stride >= 576, multiple
+ * of 8); w_uk: device bf16 [n_heads, 192, 512]; w_uv: device bf16 [n_heads,
+ * 256, 512]; k_out, v_out: device bf16 [rows, n_heads, 256] (written; rows
+ * keep the latent pool's row numbers, so the latent cache's addressing serves
+ * them).  bf16 operands, fp32 accumulation, bf16 results (round to nearest
+ * even).  All pointers 16-byte aligned; rows <= 2^31 - 1; 1 <= n_heads <=
+ * DSA_MHA_MAX_HEADS.  Asynchronous on `stream`.
+ */
+dsa_status_t dsa_mha_project(const void* latent, int64_t latent_stride, int64_t rows, int32_t n_heads,
+                             const void* w_uk, const void* w_uv, void* k_out, void* v_out, cudaStream_t stream);
+
+/* One MHA-mode attention layer. */
+typedef struct {
+  const void* q;        /* device bf16 [total_q, n_heads, 256]: per-head queries (192 no-rope + 64 rope dims) */
+  dsa_cache_t k;        /* per-head keys: rows of n_heads x 256 bf16 (row_stride >= n_heads * 256),
+                           addressed like the latent cache (contiguous or 64-token pages) */
+  dsa_cache_t v;        /* per-head values, same row numbers and the same addressing as k */
+  int32_t n_heads;      /* 1 .. DSA_MHA_MAX_HEADS */
+  int32_t head_dim;     /* DSA_MHA_HEAD_DIM */
+  int32_t v_head_dim;   /* DSA_MHA_HEAD_DIM */
+  float scale;          /* softmax scale, e.g. 1/sqrt(256) */
+} dsa_mha_layer_t;
+
+/* Workspace bytes of dsa_sparse_mha_fwd (the per-call plan and one selection
+ * bit mask per query); 0 on invalid arguments. */
+size_t dsa_mha_workspace_size(const dsa_batch_t* batch);
+
+/*
+ * dsa_sparse_mha_fwd -- for every query t and head h, softmax attention of
+ * q[t, h] over the keys k[s, h] of the selected positions s (idx[t, j] for
+ * j < min(topk, n_t); -1 entries skipped, out-of-range entries flagged
+ * DSA_ERR_BAD_INDEX and skipped):
+ *   z_s = scale * q[t, h] . k[s, h];  out[t, h] = sum_s softmax(z)_s v[s, h];
+ *   lse[t, h] = log sum_s exp(z_s).
+ * A query with no selected position gets out = 0 and lse = -inf.
+ * out: device bf16 [total_q, n_heads, 256] (written); lse: device fp32
+ * [total_q, n_heads] or NULL.  batch->max_seqlen_k <= DSA_MHA_MAX_CONTEXT.
+ * bf16 operands, fp32 accumulation and softmax, probabilities rounded to bf16
+ * for the value product.  workspace: >= dsa_mha_workspace_size(batch) bytes.
+ */
+dsa_status_t dsa_sparse_mha_fwd(const dsa_batch_t* batch, const dsa_mha_layer_t* layer, const int32_t* idx,
+                                int64_t ld_idx, int32_t topk, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * dsa_sparse_mla_fwd_noalloc -- step 3 for callers that cannot provide any
  * device memory beyond their inputs and outputs (a plugin interface that
  * hands over only tensor pointers, or an engine whose device memory is all

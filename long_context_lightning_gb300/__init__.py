@@ -6,6 +6,6 @@ with IndexShare reuse of one index set across a group of layers, and an
 HBM least-recently-used cache of latent rows over pinned host memory.
 """
 from . import _lib
-from .api import HiSparseCache, SparseAttention
+from .api import HiSparseCache, SparseAttention, SparseMHA
 
-__all__ = ["SparseAttention", "HiSparseCache", "_lib"]
+__all__ = ["SparseAttention", "SparseMHA", "HiSparseCache", "_lib"]

@@ -28,7 +28,9 @@ EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", 
            "dsa_topk", "dsa_sparse_mla_fwd", "dsa_forward", "dsa_forward_marked", "dsa_selftest_mma",
            "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
            "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_workspace_size", "dsa_hisparse_reset", "dsa_hisparse_fetch",
-           "dsa_hisparse_resident", "dsa_hisparse_stats"]
+           "dsa_hisparse_resident", "dsa_hisparse_stats", "dsa_mha_project", "dsa_mha_workspace_size",
+           "dsa_sparse_mha_fwd"]
+MHA_HEAD_DIM = 256
 NOALLOC_MAX_QUERIES = 4096
 
 
@@ -50,6 +52,11 @@ class Indexer(ctypes.Structure):
 class MlaLayer(ctypes.Structure):
     _fields_ = [("q", c_void_p), ("kv", Cache), ("n_heads", c_int32), ("d_qk", c_int32), ("d_v", c_int32),
                 ("scale", c_float)]
+
+
+class MhaLayer(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", Cache), ("v", Cache), ("n_heads", c_int32), ("head_dim", c_int32),
+                ("v_head_dim", c_int32), ("scale", c_float)]
 
 
 class HiSparse(ctypes.Structure):
@@ -123,6 +130,14 @@ def load() -> ctypes.CDLL:
     lib.dsa_hisparse_resident.argtypes = [POINTER(HiSparse), c_void_p, c_void_p]
     lib.dsa_hisparse_stats.restype = c_int32
     lib.dsa_hisparse_stats.argtypes = [POINTER(HiSparse), POINTER(c_int32), c_void_p]
+    lib.dsa_mha_project.restype = c_int32
+    lib.dsa_mha_project.argtypes = [c_void_p, c_int64, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p]
+    lib.dsa_mha_workspace_size.restype = c_size_t
+    lib.dsa_mha_workspace_size.argtypes = [POINTER(Batch)]
+    lib.dsa_sparse_mha_fwd.restype = c_int32
+    lib.dsa_sparse_mha_fwd.argtypes = [POINTER(Batch), POINTER(MhaLayer), c_void_p, c_int64, c_int32, c_void_p,
+                                       c_void_p, c_void_p, c_size_t, c_void_p]
     lib.dsa_selftest_timeout.restype = c_int32
     lib.dsa_selftest_timeout.argtypes = [c_int32, c_void_p]
     _lib = lib
@@ -316,6 +331,35 @@ def hisparse_stats(hs: HiSparse, stream=None) -> list:
     out = (c_int32 * 8)()
     _check(load().dsa_hisparse_stats(ctypes.byref(hs), out, _stream(stream)), "dsa_hisparse_stats")
     return list(out)
+
+
+def mha_project(latent: torch.Tensor, w_uk: torch.Tensor, w_uv: torch.Tensor, k_out: torch.Tensor,
+                v_out: torch.Tensor, stream=None):
+    """Per-head keys/values of every row of a latent pool (bf16 [rows, >= 576])."""
+    assert latent.dtype == torch.bfloat16 and latent.stride(1) == 1
+    for t in (w_uk, w_uv, k_out, v_out):
+        assert t.dtype == torch.bfloat16 and t.is_contiguous()
+    _check(load().dsa_mha_project(_ptr(latent), latent.stride(0), latent.shape[0], w_uk.shape[0], _ptr(w_uk),
+                                  _ptr(w_uv), _ptr(k_out), _ptr(v_out), _stream(stream)), "dsa_mha_project")
+
+
+def make_mha_layer(q: torch.Tensor, k_cache: Cache, v_cache: Cache, scale: float) -> MhaLayer:
+    assert q.dtype == torch.bfloat16 and q.is_contiguous()
+    return MhaLayer(_ptr(q), k_cache, v_cache, q.shape[1], q.shape[2], MHA_HEAD_DIM, scale)
+
+
+def mha_workspace_size(batch: Batch) -> int:
+    return int(load().dsa_mha_workspace_size(ctypes.byref(batch)))
+
+
+def sparse_mha_fwd(batch: Batch, layer: MhaLayer, idx: torch.Tensor, k: int, out: torch.Tensor,
+                   lse: Optional[torch.Tensor], workspace: torch.Tensor, stream=None):
+    assert out.dtype == torch.bfloat16 and out.is_contiguous()
+    assert idx.dtype == torch.int32 and idx.stride(1) == 1
+    _check(load().dsa_sparse_mha_fwd(ctypes.byref(batch), ctypes.byref(layer), _ptr(idx), idx.stride(0), k,
+                                     _ptr(out), _ptr(lse), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+           "dsa_sparse_mha_fwd")
 
 
 def check_device_error(stream=None) -> int:

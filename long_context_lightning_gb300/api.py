@@ -122,3 +122,38 @@ class HiSparseCache:
     def stats(self) -> dict:
         s = _lib.hisparse_stats(self.hs)
         return dict(steps=s[0], requested=s[1], hits=s[2], misses=s[3], evicted=s[4], overflow=s[5])
+
+
+class SparseMHA:
+    """MHA mode over a short context: the latent pool up-projected once into
+    per-head keys and values (`project`), then attention of every head over
+    each query's top-k selection (`forward`).  The per-head caches keep the
+    latent pool's row numbers and addressing (seq_start or page_table)."""
+
+    def __init__(self, cu_seqlens_q: torch.Tensor, seq_lens_k: torch.Tensor, latent_pool: torch.Tensor,
+                 w_uk: torch.Tensor, w_uv: torch.Tensor, scale: float, seq_start: Optional[torch.Tensor] = None,
+                 page_table: Optional[torch.Tensor] = None, page_size: int = 64):
+        dev = latent_pool.device
+        H = w_uk.shape[0]
+        rows = latent_pool.shape[0]
+        nq = (cu_seqlens_q[1:] - cu_seqlens_q[:-1]).cpu()
+        self.total_q = int(cu_seqlens_q[-1])
+        self.batch = _lib.make_batch(cu_seqlens_q, seq_lens_k, self.total_q, int(seq_lens_k.max()), int(nq.max()))
+        self.latent, self.w_uk, self.w_uv, self.scale = latent_pool, w_uk, w_uv, scale
+        self.k_pool = torch.empty((rows, H * _lib.MHA_HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.v_pool = torch.empty((rows, H * _lib.MHA_HEAD_DIM), dtype=torch.bfloat16, device=dev)
+        self.k_cache = _lib.make_cache(self.k_pool, seq_start, page_table, page_size)
+        self.v_cache = _lib.make_cache(self.v_pool, seq_start, page_table, page_size)
+        self._keep = [cu_seqlens_q, seq_lens_k, seq_start, page_table]
+        self.workspace = torch.empty(_lib.mha_workspace_size(self.batch), dtype=torch.uint8, device=dev)
+
+    def project(self, stream=None):
+        """Per-head keys and values of every latent row; asynchronous on `stream`."""
+        _lib.mha_project(self.latent, self.w_uk, self.w_uv, self.k_pool, self.v_pool, stream)
+
+    def forward(self, q: torch.Tensor, idx: torch.Tensor, k: int, out: torch.Tensor,
+                lse: Optional[torch.Tensor] = None, stream=None):
+        """out[t, h] = attention of q[t, h] (bf16 [T, H, 256]) over the selection idx[t]."""
+        layer = _lib.make_mha_layer(q, self.k_cache, self.v_cache, self.scale)
+        _lib.sparse_mha_fwd(self.batch, layer, idx, k, out, lse, self.workspace, stream)
+        return out, lse

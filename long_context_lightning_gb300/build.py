@@ -16,7 +16,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ["dsa_api.cu", "plan.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "cache_append.cu", "hisparse.cu"]
+SOURCES = ["dsa_api.cu", "plan.cu", "indexer.cu", "topk.cu", "sparse_mla.cu", "cache_append.cu", "hisparse.cu",
+           "sparse_mha.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -736,6 +736,89 @@ dsa_status_t dsa_hisparse_stats(const dsa_hisparse_t* hs, int32_t* stats, cudaSt
                                                                                                   : DSA_ERR_CUDA;
 }
 
+dsa_status_t dsa_mha_project(const void* latent, int64_t latent_stride, int64_t rows, int32_t n_heads,
+                             const void* w_uk, const void* w_uv, void* k_out, void* v_out, cudaStream_t stream) {
+  if (rows < 0 || rows > (int64_t)0x7fffffff || n_heads < 1 || n_heads > DSA_MHA_MAX_HEADS)
+    return DSA_ERR_INVALID_ARG;
+  if (latent_stride < DSA_MHA_LATENT + DSA_MHA_ROPE || latent_stride % 8 != 0) return DSA_ERR_INVALID_ARG;
+  const void* ptrs[5] = {latent, w_uk, w_uv, k_out, v_out};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;
+  DeviceInfo dev;
+  if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
+  MhaProjectLaunch a;
+  a.c = latent;
+  a.c_stride = latent_stride;
+  a.rows = rows;
+  a.H = n_heads;
+  a.w_uk = w_uk;
+  a.w_uv = w_uv;
+  a.k_out = k_out;
+  a.v_out = v_out;
+  a.err = dev.err;
+  return launch_mha_project(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+static size_t mha_mask_bytes(const dsa_batch_t* b) {
+  return align_up((size_t)b->total_q * mha_mask_words(b->max_seqlen_k) * 4, 256);
+}
+
+size_t dsa_mha_workspace_size(const dsa_batch_t* batch) {
+  if (check_batch(batch) != DSA_OK || batch->max_seqlen_k > DSA_MHA_MAX_CONTEXT) return 0;
+  return plan_bytes(batch->total_q) + mha_mask_bytes(batch);
+}
+
+dsa_status_t dsa_sparse_mha_fwd(const dsa_batch_t* batch, const dsa_mha_layer_t* layer, const int32_t* idx,
+                                int64_t ld_idx, int32_t topk, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  dsa_status_t s = check_batch(batch);
+  if (s != DSA_OK) return s;
+  if (layer == nullptr || layer->q == nullptr || !aligned16(layer->q)) return DSA_ERR_INVALID_ARG;
+  if (layer->head_dim != DSA_MHA_HEAD_DIM || layer->v_head_dim != DSA_MHA_HEAD_DIM) return DSA_ERR_UNSUPPORTED;
+  if (layer->n_heads < 1 || layer->n_heads > DSA_MHA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
+  if (batch->max_seqlen_k > DSA_MHA_MAX_CONTEXT) return DSA_ERR_UNSUPPORTED;
+  const dsa_cache_t& kc = layer->k;
+  const dsa_cache_t& vc = layer->v;
+  if (kc.kind == DSA_CACHE_ROWS || vc.kind != kc.kind || vc.num_rows != kc.num_rows ||
+      vc.seq_start != kc.seq_start || vc.page_table != kc.page_table ||
+      vc.page_table_stride != kc.page_table_stride)
+    return DSA_ERR_INVALID_ARG;
+  const int row_elems = layer->n_heads * DSA_MHA_HEAD_DIM;
+  if ((s = check_cache(kc, row_elems, batch->max_seqlen_k)) != DSA_OK) return s;
+  if ((s = check_cache(vc, row_elems, batch->max_seqlen_k)) != DSA_OK) return s;
+  if (topk < 1 || topk > DSA_MAX_TOPK) return DSA_ERR_UNSUPPORTED;
+  if (idx == nullptr || !aligned4(idx) || ld_idx < topk) return DSA_ERR_INVALID_ARG;
+  if (out == nullptr || !aligned16(out) || (lse != nullptr && !aligned4(lse))) return DSA_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < dsa_mha_workspace_size(batch))
+    return DSA_ERR_WORKSPACE;
+  if (batch->total_q == 0) return DSA_OK;
+  DeviceInfo dev;
+  if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
+  PlanView plan;
+  constexpr int kGroup = 128;  // queries per attention block
+  if ((s = run_plan(batch, kGroup, 0, workspace, dev, stream, &plan)) != DSA_OK) return s;
+  MhaAttendLaunch a;
+  a.plan = plan;
+  a.k = view_of(kc);
+  a.v = view_of(vc);
+  a.q = layer->q;
+  a.idx = idx;
+  a.ld_idx = ld_idx;
+  a.k_sel = topk;
+  a.T = batch->total_q;
+  a.H = layer->n_heads;
+  a.W = mha_mask_words(batch->max_seqlen_k);
+  a.mask = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + plan_bytes(batch->total_q));
+  a.scale = layer->scale;
+  a.out = out;
+  a.lse = lse;
+  // groups never straddle sequences: at most one partial group per sequence
+  a.max_groups = (batch->total_q + kGroup - 1) / kGroup + batch->num_seqs;
+  a.err = dev.err;
+  return launch_mha_attend(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
 dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster) {
   if (max_cluster != 0 && max_cluster != 1 && max_cluster != 2 && max_cluster != 4 && max_cluster != 8 &&
       max_cluster != 16)

@@ -198,6 +198,40 @@ cudaError_t launch_hisparse_resident(void* state, int32_t capacity, int64_t host
                                      cudaStream_t stream);
 cudaError_t hisparse_read_stats(void* state, int32_t capacity, int64_t host_rows, int32_t* out8, cudaStream_t stream);
 
+// MHA mode: per-head key/value up-projection of a latent pool, and attention
+// of every head over the selection (sparse_mha.cu).
+struct MhaProjectLaunch {
+  const void* c;      // latent pool bf16 [rows, c_stride] (512 latent + 64 rope dims)
+  int64_t c_stride;
+  int64_t rows;
+  int32_t H;
+  const void* w_uk;   // bf16 [H, 192, 512]
+  const void* w_uv;   // bf16 [H, 256, 512]
+  void* k_out;        // bf16 [rows, H, 256]
+  void* v_out;        // bf16 [rows, H, 256]
+  int* err;
+};
+struct MhaAttendLaunch {
+  PlanView plan;      // groups of up to 128 queries
+  CacheView k, v;     // per-head caches (v uses k's addressing)
+  const void* q;      // bf16 [T, H, 256]
+  const int32_t* idx;
+  int64_t ld_idx;
+  int32_t k_sel;
+  int32_t T;
+  int32_t H;
+  int32_t W;          // mask words per query
+  uint32_t* mask;     // [T, W] (workspace)
+  float scale;
+  void* out;          // bf16 [T, H, 256]
+  float* lse;
+  int32_t max_groups;
+  int* err;
+};
+int mha_mask_words(int max_seqlen_k);
+cudaError_t launch_mha_project(const MhaProjectLaunch& a, cudaStream_t stream);
+cudaError_t launch_mha_attend(const MhaAttendLaunch& a, cudaStream_t stream);
+
 // Largest thread-block cluster (8, or 16 where the device schedules it) for
 // kernel `kern` launched with `threads` threads and `smem` bytes of dynamic
 // shared memory, on the current device.  Probed once per (device, slot) under

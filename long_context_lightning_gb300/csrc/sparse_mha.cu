@@ -1,0 +1,617 @@
+// sparse_mha.cu -- MHA mode of sparse attention: per-head keys and values
+// up-projected from the latent rows, softmax attention of every head over the
+// top-k selection of its query.
+//
+// "How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
+// Model, second bullet: sparse MLA runs in MQA mode, and vLLM switches to MHA
+// mode for contexts of about 2K-5K tokens.  MQA mode reads one 576-dim latent
+// row per selected token with the up-projections absorbed into the query and
+// the output; MHA mode up-projects every token of a short context once and
+// attends with per-head keys (192 no-rope dims + the 64 shared rope dims) and
+// values (256 dims), which pays off when many queries -- a prefill chunk --
+// share that context.
+//
+// Three kernels:
+//   project  K[r, h] = (W_UK[h] c[r, :512], c[r, 512:576]) and
+//            V[r, h] = W_UV[h] c[r, :512] for every row r of a latent pool: a
+//            tcgen05 GEMM per (128 rows, head), A = the latent rows (TMA,
+//            128-byte swizzle), B = the head's projection rows, fp32 in TMEM,
+//            bf16 rows written by the epilogue (keys also copy the rope dims)
+//   mask     the selection of every query as a bit mask over its positions
+//            (one block per query, built in shared memory)
+//   attend   one block per (group of up to 128 consecutive queries of one
+//            sequence, head), keys in tiles of 64 positions (one 64-token
+//            page): S = Q K^T (M = 128 queries, N = 64 keys, K = 256) into one
+//            of two TMEM buffers, online softmax in fp32 over the selected
+//            keys only (a per-row reference that moves when a score passes it
+//            by more than 2^8, so O is rescaled in TMEM only then), P in bf16
+//            to shared memory, O += P V (M = 128, N = 256, K = 64) in TMEM.
+//            Warp 0 streams Q once and K/V tiles through two stages with TMA,
+//            warp 1 issues the MMAs, warps 2-5 own one query row per thread.
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int kLatent = 512;  // latent dims the projections read (the rest are rope dims)
+constexpr int kRope = 64;
+constexpr int kHead = 256;    // per-head q/k dims (no-rope + rope) and value dims of the kernels
+
+// ------------------------------------------------------------ project ---
+
+template <int N>
+struct ProjCfg {
+  static constexpr int STAGES = 4;
+  static constexpr int KB = kLatent / 64;        // 64-dim K blocks
+  static constexpr int A_BYTES = 128 * 128;      // 128 rows x 64 dims
+  static constexpr int B_BYTES = N * 128;        // N outputs x 64 dims
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static_assert(N % 16 == 0 && N <= 256, "tcgen05 M=128 needs N in [16, 256]");
+};
+
+struct ProjParams {
+  const __nv_bfloat16* c;  // latent pool [rows, c_stride]
+  int64_t c_stride;
+  int64_t rows;
+  int32_t H;
+  __nv_bfloat16* out;      // [rows, H, kHead]
+  int* err;
+};
+
+template <int N, bool KEYS>
+__global__ void __launch_bounds__(128, 1)
+    mha_project_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_w,
+                       ProjParams p) {
+  using C = ProjCfg<N>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (2 * C::STAGES + 2));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  auto full = [&](int s) { return smem_u32(bars + s); };
+  auto empty = [&](int s) { return smem_u32(bars + C::STAGES + s); };
+  const uint32_t done = smem_u32(bars + 2 * C::STAGES);
+  const uint32_t drain = smem_u32(bars + 2 * C::STAGES + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = blockIdx.x * 128, h = blockIdx.y;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_c);
+    prefetch_tmap(&tm_w);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 256);
+    tmem_relinquish();
+  }
+  pdl_wait();  // the latent pool may come from the previous kernel on the stream
+  pdl_trigger();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    int issued = 0;
+    for (int kb = 0; kb < C::KB; ++kb) {
+      const int s = kb % C::STAGES;
+      if (kb >= C::STAGES && !mbar_wait(empty(s), ((kb / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
+      const uint32_t dst = sbase + s * C::STAGE_BYTES;
+      mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+      tma_load_2d(dst, &tm_c, full(s), kb * 64, r0);
+      tma_load_2d(dst + C::A_BYTES, &tm_w, full(s), kb * 64, h * N);
+      ++issued;
+    }
+    if (*abort_flag)  // the loads already issued land before the block leaves
+      for (int kb = std::max(0, issued - C::STAGES); kb < issued; ++kb)
+        mbar_wait_drain(full(kb % C::STAGES), (kb / C::STAGES) & 1);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = mma_idesc_bf16(128, N, false, false);
+    bool ok = true;
+    for (int kb = 0; kb < C::KB && ok; ++kb) {
+      const int s = kb % C::STAGES;
+      if (!(ok = mbar_wait(full(s), (kb / C::STAGES) & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      const uint32_t a0 = sbase + s * C::STAGE_BYTES, b0 = a0 + C::A_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem, smem_desc_sw128(a0 + ks * 32, 16, 1024), smem_desc_sw128(b0 + ks * 32, 16, 1024), idesc,
+                 (kb | ks) != 0);
+      mma_commit(empty(s));
+    }
+    if (ok) mma_commit(done);
+    mma_commit(drain);  // every MMA of this thread done before TMEM is freed
+    mbar_wait_drain(drain, 0);
+  }
+  __syncwarp();
+
+  // epilogue: thread = one row of the tile (TMEM lane)
+  const bool ok = mbar_wait(done, 0, abort_flag, p.err);
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  const int64_t r = (int64_t)r0 + row;
+  if (ok) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
+      tmem_wait_ld();
+      if (r < p.rows) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+      }
+    }
+    if (KEYS && r < p.rows) {  // the rope dims every head shares follow the head's no-rope dims
+      const uint4* src = reinterpret_cast<const uint4*>(p.c + r * p.c_stride + kLatent);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + N);
+#pragma unroll
+      for (int i = 0; i < kRope / 8; ++i) dst[i] = __ldg(src + i);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ---------------------------------------------------------------- mask ---
+
+struct MaskParams {
+  const int32_t* idx;
+  int64_t ld_idx;
+  int32_t k;
+  int32_t T;
+  int32_t W;  // words per query row
+  const int32_t* q_n;
+  uint32_t* mask;
+  int* err;
+};
+
+__global__ void __launch_bounds__(256) mha_mask_kernel(MaskParams p) {
+  extern __shared__ uint32_t bits[];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  for (int i = threadIdx.x; i < p.W; i += blockDim.x) bits[i] = 0;
+  __syncthreads();
+  const int n_t = p.q_n[t];
+  const int m = min(n_t, p.k);
+  for (int j = threadIdx.x; j < m; j += blockDim.x) {
+    const int pos = p.idx[(int64_t)t * p.ld_idx + j];
+    if (pos == -1) continue;
+    if (pos < -1 || pos >= n_t) {
+      atomicOr(p.err, DEV_ERR_BAD_INDEX);
+      continue;
+    }
+    atomicOr(bits + (pos >> 5), 1u << (pos & 31));
+  }
+  __syncthreads();
+  uint32_t* dst = p.mask + (int64_t)t * p.W;
+  for (int i = threadIdx.x; i < p.W; i += blockDim.x) dst[i] = bits[i];
+}
+
+// -------------------------------------------------------------- attend ---
+
+struct AttCfg {
+  static constexpr int THREADS = 192;
+  static constexpr int Q_BYTES = 128 * kHead * 2;        // 64 KB: 4 blocks [128 x 64]
+  static constexpr int K_BYTES = 64 * kHead * 2;         // 32 KB: 4 blocks [64 x 64]
+  static constexpr int V_BYTES = 64 * kHead * 2;         // 32 KB: 4 value blocks [64 keys x 64]
+  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
+  static constexpr int P_BYTES = 128 * 64 * 2;           // 16 KB: [128 queries x 64 keys]
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
+  static constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int N_BARS = 12;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+  static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
+  static constexpr int TMEM_COLS = 512;                  // O: 256 columns, S: two buffers of 64
+  static constexpr uint32_t S_COL = 256;
+};
+
+struct AttParams {
+  PlanView plan;
+  CacheView kv;           // addressing of the per-head key / value caches (rows of H x 256)
+  const uint32_t* mask;
+  int32_t W;
+  int32_t H;
+  float scale_log2;
+  __nv_bfloat16* out;     // [T, H, kHead]
+  float* lse;             // [T, H] or null
+  int* err;
+};
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+__global__ void __launch_bounds__(AttCfg::THREADS, 1)
+    mha_attend_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, AttParams p) {
+  using C = AttCfg;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const uint32_t q_full = smem_u32(bars + 0);
+  auto kv_full = [&](int s) { return smem_u32(bars + 1 + s); };
+  auto kv_empty = [&](int s) { return smem_u32(bars + 3 + s); };
+  auto s_full = [&](int u) { return smem_u32(bars + 5 + u); };
+  auto s_free = [&](int u) { return smem_u32(bars + 7 + u); };
+  const uint32_t p_full = smem_u32(bars + 9);
+  const uint32_t pv_done = smem_u32(bars + 10);
+  const uint32_t drain = smem_u32(bars + 11);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait();  // the plan and the masks are complete from here on
+  pdl_trigger();
+  const int g = blockIdx.x, h = blockIdx.y;
+  if (g >= p.plan.header[0]) return;  // the grid is sized for the most groups a batch can have
+  const int4 gi = p.plan.g_info[g];   // {sequence, first query, queries, n of the last query}
+  const int b = gi.x, q0 = gi.y, cnt = gi.z;
+  const int n_kt = (gi.w + 63) / 64;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+      mbar_init(s_full(s), 1);
+      mbar_init(s_free(s), 128);
+    }
+    mbar_init(p_full, 128);
+    mbar_init(pv_done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  // value stages start as zeros: a key that no query selects contributes P = 0
+  // times whatever its stage holds, which must not be a NaN pattern
+  for (int i = threadIdx.x; i < 2 * C::V_BYTES / 16; i += C::THREADS) {
+    const int s = i / (C::V_BYTES / 16), o = i % (C::V_BYTES / 16);
+    st_shared_v4(sbase + C::OFF_KV + s * C::STAGE_BYTES + C::K_BYTES + o * 16, 0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_kt > 0) {
+      mbar_arrive_expect_tx(q_full, C::Q_BYTES);
+      for (int kb = 0; kb < 4; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 16384, &tm_q, q_full, kb * 64, h, q0);
+      int issued = 0;
+      for (int j = 0; j < n_kt; ++j) {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(kv_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) break;
+        int64_t row0;
+        bool valid = true;
+        if (p.kv.paged) {  // a 64-key tile is one 64-token page
+          const int64_t phys = __ldg(p.kv.page_table + (int64_t)b * p.kv.pt_stride + j);
+          valid = phys >= 0 && (phys + 1) * 64 <= p.kv.num_rows;
+          row0 = phys * 64;
+        } else {
+          row0 = __ldg(p.kv.seq_start + b) + (int64_t)j * 64;
+          valid = row0 >= 0 && row0 < p.kv.num_rows;
+        }
+        const uint32_t dst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
+        if (valid) {
+          mbar_arrive_expect_tx(kv_full(s), C::STAGE_BYTES);
+          for (int kb = 0; kb < 4; ++kb) {
+            tma_load_3d(dst + kb * 8192, &tm_k, kv_full(s), kb * 64, h, (int32_t)row0);
+            tma_load_3d(dst + C::K_BYTES + kb * 8192, &tm_v, kv_full(s), kb * 64, h, (int32_t)row0);
+          }
+        } else {
+          atomicOr(p.err, DEV_ERR_BAD_INDEX);
+          mbar_arrive(kv_full(s));  // nothing loaded: the stage keeps earlier (finite) contents
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait_drain(q_full, 0);
+        for (int j = std::max(0, issued - 2); j < issued; ++j) mbar_wait_drain(kv_full(j & 1), (j >> 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_kt > 0) {
+      const uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
+      const uint32_t idesc_o = mma_idesc_bf16(128, kHead, false, true);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
+      auto issue_s = [&](int j) -> bool {
+        const int u = j & 1;
+        if (!mbar_wait(kv_full(u), (j >> 1) & 1, abort_flag, p.err)) return false;
+        if (j >= 2 && !mbar_wait(s_free(u), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
+        tc_fence_after();
+        const uint32_t kbase = sbase + C::OFF_KV + u * C::STAGE_BYTES;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + C::S_COL + u * 64, smem_desc_sw128(sbase + C::OFF_Q + kb * 16384 + ks * 32, 16, 1024),
+                     smem_desc_sw128(kbase + kb * 8192 + ks * 32, 16, 1024), idesc_s, (kb | ks) != 0);
+        mma_commit(s_full(u));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; j < n_kt && ok; ++j) {
+        if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
+        if (!(ok = mbar_wait(p_full, j & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        const uint32_t vbase = sbase + C::OFF_KV + (j & 1) * C::STAGE_BYTES + C::K_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem, smem_desc_sw128(sbase + C::OFF_P + ks * 32, 16, 1024),
+                   smem_desc_sw128(vbase + ks * 2048, 8192, 1024), idesc_o, (j | ks) != 0);
+        mma_commit(kv_empty(j & 1));
+        mma_commit(pv_done);
+      }
+      mma_commit(drain);  // every MMA of this thread done before TMEM is freed
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // -------------------------------------------- softmax, one row per thread
+    const int qd = warp & 3;
+    const int row = qd * 32 + lane;
+    const int t = q0 + row;
+    const bool valid_q = row < cnt;
+    const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+    const uint32_t* mrow = p.mask + (int64_t)(valid_q ? t : 0) * p.W;
+    float m_ref = neg_inf(), l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int u = j & 1;
+      if (!(ok = mbar_wait(s_full(u), (j >> 1) & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      uint32_t sv[64];
+      {
+        uint32_t a[32], c[32];
+        tmem_ld32(tmem + lane_base + C::S_COL + u * 64, a);
+        tmem_ld32(tmem + lane_base + C::S_COL + u * 64 + 32, c);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          sv[i] = a[i];
+          sv[32 + i] = c[i];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free(u));
+      const uint2 bits = valid_q ? *reinterpret_cast<const uint2*>(mrow + 2 * j) : make_uint2(0u, 0u);
+      float x[64];
+      float mt = neg_inf();
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const uint32_t bit = ((c < 32 ? bits.x : bits.y) >> (c & 31)) & 1u;
+        x[c] = bit ? __uint_as_float(sv[c]) * p.scale_log2 : neg_inf();
+        mt = fmaxf(mt, x[c]);
+      }
+      // the P buffer and O are the previous PV's until it completes
+      if (j > 0 && !(ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.err))) break;
+      tc_fence_after();
+      // the reference moves when a score passes it by more than 2^8; O and l
+      // follow it (TMEM loads and stores are warp-wide: a row that keeps its
+      // reference is scaled by 1)
+      const bool move = mt > m_ref + 8.f;
+      const bool need = move && j > 0 && l > 0.f;
+      const float f = need ? ex2_approx(m_ref - mt) : 1.f;
+      const bool rescaled = __any_sync(0xffffffffu, need);
+      if (rescaled) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < kHead; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + c0, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tmem_st32(tmem + lane_base + c0, o);
+        }
+      }
+      l *= f;
+      if (move) m_ref = mt;
+      float lsum = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = x[c] == neg_inf() ? 0.f : ex2_approx(x[c] - m_ref);
+        const float p1 = x[c + 1] == neg_inf() ? 0.f : ex2_approx(x[c + 1] - m_ref);
+        const uint32_t w = pack_bf16x2(p0, p1);
+        lsum += bf16lo_to_f32(w) + bf16hi_to_f32(w);
+        pk[c >> 1] = w;
+      }
+      l += lsum;
+      const uint32_t prow = sbase + C::OFF_P + row * 128;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      fence_proxy_async_smem();
+      if (rescaled) tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && n_kt > 0) ok = mbar_wait(pv_done, (n_kt - 1) & 1, abort_flag, p.err);
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int64_t orow = (int64_t)t * p.H + h;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kHead; c0 += 32) {
+      uint32_t o[32];
+      if (n_kt > 0) {
+        tmem_ld32(tmem + lane_base + c0, o);
+        tmem_wait_ld();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (valid_q && ok) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + orow * kHead + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(o[8 * i]) * inv, __uint_as_float(o[8 * i + 1]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv, __uint_as_float(o[8 * i + 3]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv, __uint_as_float(o[8 * i + 5]) * inv),
+                              pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
+      }
+    }
+    if (valid_q && ok && p.lse != nullptr)
+      p.lse[orow] = l > 0.f ? (m_ref + lg2_approx(l)) * 0.69314718055994531f : neg_inf();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+cudaError_t launch_with(const void* kern, dim3 grid, int block, size_t smem, void** args, cudaStream_t stream,
+                        bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at = pdl_attribute();
+  cfg.attrs = &at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+template <int N, bool KEYS>
+cudaError_t launch_project_one(const MhaProjectLaunch& a, const void* w, __nv_bfloat16* out, cudaStream_t stream) {
+  using C = ProjCfg<N>;
+  CUtensorMap tm_c, tm_w;
+  {
+    const uint64_t dims[2] = {(uint64_t)(kLatent + kRope), (uint64_t)a.rows};
+    const uint64_t strides[1] = {(uint64_t)a.c_stride * 2};
+    const uint32_t box[2] = {64, 128};
+    if (encode_tmap(&tm_c, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.c, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)kLatent, (uint64_t)a.H * N};
+    const uint64_t strides[1] = {(uint64_t)kLatent * 2};
+    const uint32_t box[2] = {64, (uint32_t)N};
+    if (encode_tmap(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  ProjParams p;
+  p.c = static_cast<const __nv_bfloat16*>(a.c);
+  p.c_stride = a.c_stride;
+  p.rows = a.rows;
+  p.H = a.H;
+  p.out = out;
+  p.err = a.err;
+  auto kern = mha_project_kernel<N, KEYS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&tm_c, &tm_w, &p};
+  const dim3 grid((unsigned)((a.rows + 127) / 128), (unsigned)a.H, 1);
+  return launch_with(reinterpret_cast<const void*>(kern), grid, 128, C::SMEM_BYTES, args, stream, true);
+}
+
+}  // namespace
+
+cudaError_t launch_mha_project(const MhaProjectLaunch& a, cudaStream_t stream) {
+  if (a.rows <= 0) return cudaSuccess;
+  cudaError_t e = launch_project_one<kHead - kRope, true>(a, a.w_uk, static_cast<__nv_bfloat16*>(a.k_out), stream);
+  if (e != cudaSuccess) return e;
+  return launch_project_one<kHead, false>(a, a.w_uv, static_cast<__nv_bfloat16*>(a.v_out), stream);
+}
+
+int mha_mask_words(int max_seqlen_k) { return ((max_seqlen_k + 31) / 32 + 1) / 2 * 2; }
+
+cudaError_t launch_mha_attend(const MhaAttendLaunch& a, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  // (1) selection masks
+  MaskParams mp;
+  mp.idx = a.idx;
+  mp.ld_idx = a.ld_idx;
+  mp.k = a.k_sel;
+  mp.T = a.T;
+  mp.W = a.W;
+  mp.q_n = a.plan.q_n;
+  mp.mask = a.mask;
+  mp.err = a.err;
+  {
+    void* args[] = {&mp};
+    const size_t smem = (size_t)a.W * 4;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(mha_mask_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    cudaError_t e = launch_with(reinterpret_cast<const void*>(mha_mask_kernel), dim3(a.T, 1, 1), 256, smem, args,
+                                stream, true);
+    if (e != cudaSuccess) return e;
+  }
+  // (2) attention
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    const uint64_t dims[3] = {(uint64_t)kHead, (uint64_t)a.H, (uint64_t)a.T};
+    const uint64_t strides[2] = {(uint64_t)kHead * 2, (uint64_t)kHead * a.H * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (encode_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const CacheView* views[2] = {&a.k, &a.v};
+  CUtensorMap* maps[2] = {&tm_k, &tm_v};
+  for (int i = 0; i < 2; ++i) {
+    const uint64_t dims[3] = {(uint64_t)kHead, (uint64_t)a.H, (uint64_t)views[i]->num_rows};
+    const uint64_t strides[2] = {(uint64_t)kHead * 2, (uint64_t)views[i]->row_stride * 2};
+    const uint32_t box[3] = {64, 1, 64};
+    if (encode_tmap(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, views[i]->base, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  AttParams p;
+  p.plan = a.plan;
+  p.kv = a.k;
+  p.mask = a.mask;
+  p.W = a.W;
+  p.H = a.H;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.err = a.err;
+  cudaError_t e = cudaFuncSetAttribute(mha_attend_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       AttCfg::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&tm_q, &tm_k, &tm_v, &p};
+  const dim3 grid((unsigned)a.max_groups, (unsigned)a.H, 1);
+  return launch_with(reinterpret_cast<const void*>(mha_attend_kernel), grid, AttCfg::THREADS, AttCfg::SMEM_BYTES,
+                     args, stream, true);
+}
+
+}  // namespace dsa
