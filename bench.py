@@ -20,7 +20,9 @@ L2 flushed between steps) with its dominant kernel's roofline and the oracle
 timed on a bounded sample beside it.  For IndexShare one query token is one
 query through the whole 4-layer group.  `per_config.hisparse` times the HBM
 row cache over pinned host memory on the decode workload (cold, warm and
-decode-like steps) and sparse MLA over its slots.
+decode-like steps) and sparse MLA over its slots.  `per_config.mha` times MHA mode
+(per-head up-projection of a 4608-token context and attention of 64 heads
+over each query's selection) on its prefill-chunk workload.
 """
 from __future__ import annotations
 
@@ -437,6 +439,7 @@ def run_gpu(args, rank, world, local_rank):
     if not args.no_per_config:
         per_config = _per_config(args, dev, stream, flush_l2, peaks)
         per_config["hisparse"] = _hisparse(args, dev, stream, flush_l2)
+        per_config["mha"] = _mha_config(args, dev, stream, flush_l2, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": "query tokens/s", "n_gpus": world, "steps": args.steps,
@@ -593,6 +596,108 @@ def _hisparse(args, dev, stream, flush_l2):
         "launches_per_fetch": 7,
         "cpu_baseline": {"value": sum(len(r) for r in reqs) / dt, "unit": "requested rows/s", "kind": "oracle",
                          "cores": 1, "sample": f"LRU bookkeeping of the {len(reqs)}-step trace, python, {dt:.2f} s"},
+    }
+
+
+def _mha_config(args, dev, stream, flush_l2, peaks):
+    """MHA mode on its workload (one sequence, context 4608, 3072 queries of
+    which 512 see at most 2048 tokens): indexer -> top-k -> per-head
+    up-projection of the 4608 latent rows -> attention of every head over its
+    selection, replayed from a CUDA graph, L2 flushed between steps."""
+    import oracle
+    from long_context_lightning_gb300 import SparseMHA, _lib
+    from long_context_lightning_gb300 import accounting as A
+    spec = W.SPECS["mha"]
+    run = _Run(spec, dev)
+    wl, sa = run.wl, run.sa
+    T, H, k = wl.total_q, spec.heads, spec.topk
+    mha = SparseMHA(wl.cu_seqlens_q, wl.seq_lens, wl.kv[0], wl.w_uk[0], wl.w_uv[0], spec.scale,
+                    seq_start=wl.seq_start)
+    scores = sa.scores_view()
+    out = torch.empty((T, H, 256), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    q = wl.q_mha[0]
+
+    calls = [lambda: _lib.indexer_scores(sa.batch, sa.indexer, scores, sa.workspace),
+             lambda: _lib.topk(sa.batch, scores, k, sa.idx, sa.workspace),
+             lambda: mha.project(),
+             lambda: mha.forward(q, sa.idx, k, out, lse)]
+    for c in calls:
+        c()
+    torch.cuda.synchronize(dev)
+    run.check("mha")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        for c in calls:
+            c()
+    steps = max(3, min(args.steps, 20))
+    for _ in range(3):
+        graph.replay()
+    ev = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+    step_ms = []
+    per = [[] for _ in calls]
+    for i in range(steps):
+        flush_l2(i)
+        a, b = ev(), ev()
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        step_ms.append(a.elapsed_time(b))
+    for i in range(steps):
+        flush_l2(i)
+        marks = [ev() for _ in range(len(calls) + 1)]
+        marks[0].record(stream)
+        for j, c in enumerate(calls):
+            c()
+            marks[j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        for j in range(len(calls)):
+            per[j].append(marks[j].elapsed_time(marks[j + 1]))
+    run.check("mha timing")
+    names = ["indexer", "topk", "mha_project", "mha_attend"]
+    kern_ms = {n: statistics.mean(v) for n, v in zip(names, per)}
+    ms = statistics.mean(step_ms)
+    hbm, tf_burst, tf_sust, kind = peaks
+    shp = _shape(wl)
+    att_f = A.mha_attend_flops(shp)
+    proj_f = A.mha_project_flops(int(wl.kv[0].shape[0]), H)
+    # executed FLOPs of the attention: every 64-key tile up to the last query of a 128-query group
+    seq, pos = wl.query_positions()
+    exec_f = 0
+    for g0 in range(0, T, 128):
+        n_last = pos[min(T, g0 + 128) - 1] + 1
+        exec_f += 128 * ((n_last + 63) // 64) * 64 * H * (256 + 256) * 2
+    att_tf = att_f / (kern_ms["mha_attend"] * 1e-3) / 1e12
+    proj_tf = proj_f / (kern_ms["mha_project"] * 1e-3) / 1e12
+    cpu = wl.to("cpu")
+    t0 = time.perf_counter()
+    done = 0
+    sample = [T - 1, 0, T // 2, 100]
+    while time.perf_counter() - t0 < 2.0 or done < 2:
+        t = sample[done % len(sample)]
+        sel = oracle.dsa_forward(cpu, queries=[t], layers=[]).idx[t]
+        oracle.mha_attention_on_set(cpu, t, 0, sel)
+        done += 1
+    dt = time.perf_counter() - t0
+    del run, mha
+    torch.cuda.empty_cache()
+    return {
+        "workload": f"mha: B=1 x ctx {spec.ctx_len}, {spec.q_per_seq} queries (positions {spec.ctx_len - spec.q_per_seq}"
+                    f"..{spec.ctx_len - 1}); indexer {spec.idx_heads}x{spec.idx_dim}; top-k {k}; {H} heads, keys "
+                    f"192 up-projected + 64 rope dims, values 256 up-projected, from the 576-dim latent",
+        "value": T / (ms * 1e-3), "unit": "query tokens/s", "ms_per_step": ms, "steps": steps,
+        "kernels_ms": kern_ms,
+        "roofline": {"bound": "tensor", "kernel": "mha_attend", "achieved": att_tf, "peak": tf_sust,
+                     "unit": "TFLOP/s", "frac": att_tf / tf_sust, "traffic": None,
+                     "peak_kind": f"{kind} (bf16 sustained)", "algorithmic_flops_per_launch": att_f,
+                     "executed_flops_per_launch": exec_f,
+                     "executed_tflops": exec_f / (kern_ms["mha_attend"] * 1e-3) / 1e12},
+        "mha_project": {"tflops": proj_tf, "frac": proj_tf / tf_sust, "flops_per_launch": proj_f},
+        "cpu_baseline": {"value": done / dt, "unit": "query tokens/s", "kind": "oracle",
+                         "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+                         "sample": f"{done} queries (indexer + top-k + per-head up-projection of the selected rows + "
+                                   f"64-head attention), float64 numpy, {dt:.1f} s"},
     }
 
 

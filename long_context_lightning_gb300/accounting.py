@@ -85,3 +85,21 @@ def forward_bytes(s: Shape, unique_rows_per_seq=None) -> int:
 
 def forward_flops(s: Shape) -> int:
     return indexer_flops(s) + mla_flops(s)
+
+
+# MHA mode: every latent row of the context up-projected once into per-head
+# keys (d_nope dims + the shared rope dims) and values (d_vh dims), then each
+# head attends with its own query over the selection.
+def mha_project_flops(rows: int, heads: int, d_latent: int = 512, d_nope: int = 192, d_vh: int = 256) -> int:
+    return 2 * rows * heads * (d_nope + d_vh) * d_latent
+
+
+def mha_project_bytes(rows: int, heads: int, d_row: int = 576, d_latent: int = 512, d_nope: int = 192,
+                      d_vh: int = 256, d_head: int = 256) -> int:
+    """Latent rows read, projection weights read, per-head key and value rows written."""
+    return rows * d_row * 2 + heads * (d_nope + d_vh) * d_latent * 2 + rows * heads * 2 * d_head * 2
+
+
+def mha_attend_flops(s: Shape, d_head: int = 256, d_vh: int = 256) -> int:
+    """Q.K and P.V over the selected positions only (m_t = min(n_t, k) per query)."""
+    return sum(2 * s.heads * min(n, s.topk) * (d_head + d_vh) for n in s.n)
