@@ -432,6 +432,12 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  * 16; 0 restores the default), so tests can drive the paths taken when a row
  * is split over fewer blocks (long per-thread runs).  Host state only.
  *
+ * dsa_selftest_topk_path: with `candidates` = 0 the top-k always takes its
+ * three-pass path (every digit summed across the cluster, every block writes
+ * its own selections); 1 (the default) lets it finish from the first digit's
+ * candidates in one block when they fit.  Both give the same indices; tests
+ * compare them.  Host state of the current device only.
+ *
  * dsa_selftest_timeout: launches one block that waits on a barrier nobody
  * arrives at; the bounded wait gives up after about `limit_ms` milliseconds
  * and sets the device error word, which dsa_check_device_error then reports
@@ -440,6 +446,7 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
                               int32_t swizzle_bytes, cudaStream_t stream);
 dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster);
+dsa_status_t dsa_selftest_topk_path(int32_t candidates);
 dsa_status_t dsa_selftest_timeout(int32_t limit_ms, cudaStream_t stream);
 
 #ifdef __cplusplus

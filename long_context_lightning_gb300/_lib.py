@@ -29,7 +29,7 @@ EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", 
            "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
            "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_workspace_size", "dsa_hisparse_reset", "dsa_hisparse_fetch",
            "dsa_hisparse_resident", "dsa_hisparse_stats", "dsa_mha_project", "dsa_mha_workspace_size",
-           "dsa_sparse_mha_fwd"]
+           "dsa_sparse_mha_fwd", "dsa_selftest_topk_path"]
 MHA_HEAD_DIM = 256
 NOALLOC_MAX_QUERIES = 4096
 
@@ -138,6 +138,8 @@ def load() -> ctypes.CDLL:
     lib.dsa_sparse_mha_fwd.restype = c_int32
     lib.dsa_sparse_mha_fwd.argtypes = [POINTER(Batch), POINTER(MhaLayer), c_void_p, c_int64, c_int32, c_void_p,
                                        c_void_p, c_void_p, c_size_t, c_void_p]
+    lib.dsa_selftest_topk_path.restype = c_int32
+    lib.dsa_selftest_topk_path.argtypes = [c_int32]
     lib.dsa_selftest_timeout.restype = c_int32
     lib.dsa_selftest_timeout.argtypes = [c_int32, c_void_p]
     _lib = lib
@@ -376,6 +378,11 @@ def selftest_mma(a: torch.Tensor, b: torch.Tensor, d: torch.Tensor, a_mn_major: 
 def selftest_topk_max_cluster(max_cluster: int):
     """Cap the top-k cluster size on the current device (0 restores the default)."""
     _check(load().dsa_selftest_topk_max_cluster(max_cluster), "dsa_selftest_topk_max_cluster")
+
+
+def selftest_topk_path(candidates: bool):
+    """Let the top-k finish from the first digit's candidates (True, the default) or force three passes."""
+    _check(load().dsa_selftest_topk_path(1 if candidates else 0), "dsa_selftest_topk_path")
 
 
 def selftest_timeout(limit_ms: int, stream=None):

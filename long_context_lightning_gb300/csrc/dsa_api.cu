@@ -43,6 +43,7 @@ dsa_status_t device_info(DeviceInfo* out) {
 // Per-device cluster-size probes of the kernels (see max_cluster_for).
 int g_cluster_max[kMaxDevices][kClusterSlots] = {};
 int g_topk_cap[kMaxDevices] = {};
+bool g_topk_three_pass[kMaxDevices] = {};
 std::mutex g_cluster_mu;
 
 using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -240,6 +241,13 @@ int max_cluster_for(const void* kern, int threads, size_t smem, int slot) {
     m = best;
   }
   return m;
+}
+
+bool topk_three_pass_only() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  return g_topk_three_pass[dev];
 }
 
 int topk_cluster_cap() {
@@ -827,6 +835,15 @@ dsa_status_t dsa_selftest_topk_max_cluster(int32_t max_cluster) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_cluster_mu);
   g_topk_cap[dev] = max_cluster;
+  return DSA_OK;
+}
+
+dsa_status_t dsa_selftest_topk_path(int32_t candidates) {
+  if (candidates != 0 && candidates != 1) return DSA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_cluster_mu);
+  g_topk_three_pass[dev] = candidates == 0;
   return DSA_OK;
 }
 

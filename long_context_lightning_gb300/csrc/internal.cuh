@@ -241,6 +241,8 @@ enum { kClusterSlotTopk = 0, kClusterSlotMla0 = 1, kClusterSlotMla1 = 2, kCluste
 int max_cluster_for(const void* kern, int threads, size_t smem, int slot);
 // Cap on the top-k cluster size set by dsa_selftest_topk_max_cluster (0: none).
 int topk_cluster_cap();
+// Set by dsa_selftest_topk_path(0): the top-k takes the three-pass path only.
+bool topk_three_pass_only();
 
 // Tensor-map encoder (driver entry point, resolved once).
 CUresult encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t rank, const void* base,

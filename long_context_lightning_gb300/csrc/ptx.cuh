@@ -434,6 +434,15 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t v, uint32_t
                "r"(bar_cluster)
                : "memory");
 }
+__device__ __forceinline__ void st_dsmem_v2_u32(uint32_t addr, uint32_t a, uint32_t b) {  // 8-byte aligned
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+// Atomic add on a shared variable of a block of the cluster; returns the old value.
+__device__ __forceinline__ uint32_t atom_add_dsmem_u32(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void st_dsmem_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }

@@ -14,6 +14,16 @@
 // a contiguous run of the chunk and places its selections after one block scan
 // of the threads' counts.  When the chunk fits in shared memory the row is read
 // from global memory exactly once.
+//
+// Candidate path (taken when it fits, decided the same way by every block):
+// after the first digit, the keys at or above its bin -- the k selections plus
+// the rest of the threshold bin, usually a few hundred more -- are few.  Every
+// block sends its candidates, in position order, into the shared memory of
+// the cluster's first block (one atomic reserves a contiguous segment, a table
+// records it by block rank); after one more cluster barrier that block alone
+// finishes the last two digits over the candidates and writes the row in
+// position order.  Two cluster barriers instead of four, and the last two
+// digits touch only the candidates.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -24,7 +34,9 @@ namespace {
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kMaxCacheKeys = 45056;  // 176 KB of cached keys per block
+constexpr int kMaxCacheKeys = 32768;  // 128 KB of cached keys per block
+constexpr int kCand = 8192;           // candidate capacity of the first block (64 KB of (key, position))
+constexpr int kMaxCluster = 16;
 
 __device__ __forceinline__ uint32_t ordered_key(float x) {
   uint32_t u = __float_as_uint(x);
@@ -43,6 +55,7 @@ struct TopkParams {
   const int32_t* q_n;
   int* err;
   int32_t plan_early;  // the plan was written two or more grids back
+  int32_t cand;        // the first block has room for the candidate path
 };
 
 __device__ __forceinline__ int warp_excl_scan(int v) {
@@ -60,14 +73,154 @@ __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool active)
   if (active) atomicAdd(&h[bin], 1u);
 }
 
+// Block-wide exclusive scan of one int per thread (kThreads threads); returns
+// the prefix and the total.  Uses a[kWarps] and b[kWarps] as scratch.
+__device__ __forceinline__ int block_scan(int v, int* a, int* b, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ex = warp_excl_scan(v);
+  if (lane == 31) a[warp] = ex + v;
+  __syncthreads();
+  if (warp == 0) b[lane] = warp_excl_scan(a[lane]);
+  __syncthreads();
+  const int r = b[warp] + ex;
+  *total = b[kWarps - 1] + a[kWarps - 1];
+  __syncthreads();
+  return r;
+}
+
+// One block: the digit (over bins [0, nb) of histogram h) that holds the
+// rem-th largest key, and the rank left inside it.
+__device__ __forceinline__ void block_select_digit(const uint32_t* h, int nb, uint32_t rem, int* a, int* b,
+                                                   uint32_t* s_digit, uint32_t* s_rem) {
+  const int bpt = nb / kThreads;
+  const int top = nb - 1 - (int)threadIdx.x * bpt;
+  int mine = 0;
+  for (int j = 0; j < bpt; ++j) mine += (int)h[top - j];
+  int total;
+  int acc = block_scan(mine, a, b, &total);
+  if ((uint32_t)acc < rem && rem <= (uint32_t)(acc + mine)) {
+    for (int j = 0; j < bpt; ++j) {
+      const int cnt = (int)h[top - j];
+      if ((uint32_t)(acc + cnt) >= rem) {
+        *s_digit = top - j;
+        *s_rem = rem - acc;
+        break;
+      }
+      acc += cnt;
+    }
+  }
+  __syncthreads();
+}
+
+template <class Keys4>
+__device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hist, uint2* cand, bool cached, Keys4 keys4,
+                                            int len, int c0, uint32_t d0, uint32_t rem0, uint32_t own_above,
+                                            uint32_t crank, uint32_t csize, int32_t* out, int* w_a, int* w_b,
+                                            int* w_c, int* w_d, uint32_t* s_cand_n, uint32_t (*s_seg)[2],
+                                            uint32_t* s_cbase, uint32_t* s_digit, uint32_t* s_rem) {
+  (void)cached;
+  const int k = p.k;
+  // (1) this block's candidates: its keys whose first digit is d0 or above, in position order
+  const uint32_t mine = own_above + hist[d0];
+  if (threadIdx.x == 0) {
+    const uint32_t base = atom_add_dsmem_u32(dsmem_addr(smem_u32(s_cand_n), 0), mine);
+    *s_cbase = base;
+    st_dsmem_u32(dsmem_addr(smem_u32(&s_seg[crank][0]), 0), base);
+    st_dsmem_u32(dsmem_addr(smem_u32(&s_seg[crank][1]), 0), mine);
+  }
+  const int R = ((len + kThreads - 1) / kThreads + 3) & ~3;
+  const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
+  int cnt = 0;
+  for (int i = r0; i < r1; i += 4) {
+    uint32_t kk[4];
+    keys4(i, kk);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) cnt += (i + j < r1) && (kk[j] >> 21) >= d0;
+  }
+  int total;
+  const int before = block_scan(cnt, w_a, w_b, &total);  // also orders s_cbase before its use
+  uint32_t slot = *s_cbase + (uint32_t)before;
+  const uint32_t cand0 = dsmem_addr(smem_u32(cand), 0);
+  for (int i = r0; i < r1; i += 4) {
+    uint32_t kk[4];
+    keys4(i, kk);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((i + j < r1) && (kk[j] >> 21) >= d0) {
+        st_dsmem_v2_u32(cand0 + slot * 8u, kk[j], (uint32_t)(c0 + i + j));
+        ++slot;
+      }
+  }
+  cluster_sync();  // every block's candidates are in the first block; no one reads a peer's memory after this
+  if (crank != 0) return;
+
+  // (2) the first block: the last two digits among the candidates of bin d0
+  const int n_c = (int)*s_cand_n;
+  uint32_t* h1 = hist + kBins;
+  uint32_t* h2 = hist + 2 * kBins;
+  for (int i = threadIdx.x; i < n_c; i += kThreads) {
+    const uint32_t key = cand[i].x;
+    if ((key >> 21) == d0) atomicAdd(&h1[(key >> 10) & 0x7FFu], 1u);
+  }
+  __syncthreads();
+  block_select_digit(h1, kBins, rem0, w_a, w_b, s_digit, s_rem);
+  const uint32_t d1 = *s_digit, rem1 = *s_rem;
+  const uint32_t pre = (d0 << 11) | d1;
+  for (int i = threadIdx.x; i < n_c; i += kThreads) {
+    const uint32_t key = cand[i].x;
+    if ((key >> 10) == pre) atomicAdd(&h2[key & 0x3FFu], 1u);
+  }
+  __syncthreads();
+  block_select_digit(h2, 1024, rem1, w_a, w_b, s_digit, s_rem);
+  const uint32_t thr = (pre << 10) | *s_digit;  // the k-th largest key
+  const int take = (int)*s_rem;                 // keys equal to it that are selected (lowest positions first)
+
+  // (3) ordered write: segments in block-rank order, each in position order
+  int out_pos = 0, eq_taken = 0;
+  for (uint32_t r = 0; r < csize; ++r) {
+    const int sb = (int)s_seg[r][0], sc = (int)s_seg[r][1];
+    const int Rs = (sc + kThreads - 1) / kThreads;
+    const int a0 = min(sc, (int)threadIdx.x * Rs), a1 = min(sc, a0 + Rs);
+    int gt = 0, eq = 0;
+    for (int i = a0; i < a1; ++i) {
+      const uint32_t key = cand[sb + i].x;
+      gt += key > thr;
+      eq += key == thr;
+    }
+    int gt_tot, eq_tot;
+    const int gt_before = block_scan(gt, w_a, w_b, &gt_tot);
+    const int eq_before = block_scan(eq, w_c, w_d, &eq_tot);
+    const int left = take - eq_taken;
+    const int allow = max(0, min(eq, left - eq_before));
+    int pos = out_pos + gt_before + min(eq_before, max(left, 0));
+    int eq_seen = 0;
+    for (int i = a0; i < a1; ++i) {
+      const uint2 c = cand[sb + i];
+      const bool e = c.x == thr;
+      if (c.x > thr || (e && eq_seen < allow)) {
+        if (pos < k) out[pos] = (int32_t)c.y;
+        ++pos;
+      }
+      eq_seen += e;
+    }
+    const int eq_used = min(eq_tot, max(left, 0));
+    out_pos += gt_tot + eq_used;
+    eq_taken += eq_used;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* hist = sm;                    // [3][kBins] this block's digit histograms
   uint32_t* tot = sm + 3 * kBins;         // [kBins] cluster-summed histogram of the current digit
   uint32_t* cache = sm + 4 * kBins;       // [cache_keys]
+  uint2* cand = reinterpret_cast<uint2*>(cache + p.cache_keys);  // [kCand] (key, position), first block only
   __shared__ int w_gt[kWarps], w_eq[kWarps], w_eqb[kWarps], w_selb[kWarps];
   __shared__ uint32_t s_digit, s_rem, s_local_above;
   __shared__ uint32_t s_xch[2];           // this block's (keys above threshold, keys equal to it)
+  __shared__ uint32_t s_cand_n;           // first block: candidate slots reserved so far
+  __shared__ uint32_t s_seg[kMaxCluster][2];  // first block: (first slot, count) of each block's candidates
+  __shared__ uint32_t s_cbase;
 
   const int t = blockIdx.y;
   const uint32_t crank = cluster_ctarank();
@@ -93,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   const float* row = p.scores + (int64_t)t * p.ld_scores;
 
   for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) hist[i] = 0;
+  if (threadIdx.x == 0) s_cand_n = 0;  // before the first cluster barrier, so before any peer's reservation
   __syncthreads();
   auto keys4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4, i < len)
     if (cached) {
@@ -222,6 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
     local_greater += s_local_above;
     prefix = (prefix << bits) | s_digit;
     rem = s_rem;
+    if (pass == 0 && p.cand && (uint32_t)k - rem + tot[prefix] <= (uint32_t)kCand) {
+      candidate_path(p, hist, cand, cached, keys4, len, c0, prefix, rem, local_greater, crank, csize, out, w_gt,
+                     w_eq, w_selb, w_eqb, &s_cand_n, s_seg, &s_cbase, &s_digit, &s_rem);
+      return;
+    }
     __syncthreads();  // the next pass rewrites s_digit, s_rem, s_local_above and the scratch
   }
   const uint32_t thr = prefix;  // the k-th largest key
@@ -329,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
 
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  const int probe_smem = (4 * kBins + kMaxCacheKeys) * 4;
+  const int probe_smem = (4 * kBins + kMaxCacheKeys + 2 * kCand) * 4;
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, probe_smem);
   if (e != cudaSuccess) return e;
   int max_cluster = max_cluster_for(reinterpret_cast<const void*>(topk_kernel), kThreads, probe_smem,
@@ -343,7 +502,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   while (c < max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
   const int per = (((a.max_n + c - 1) / c) + 3) & ~3;
   const int cache_keys = per <= kMaxCacheKeys ? per : 0;
-  const size_t smem = (size_t)(4 * kBins + cache_keys) * 4;
+  const size_t smem = (size_t)(4 * kBins + cache_keys + 2 * kCand) * 4;
   e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
 
@@ -358,6 +517,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   p.q_n = a.q_n;
   p.err = a.err;
   p.plan_early = a.plan_early ? 1 : 0;
+  p.cand = (c <= kMaxCluster && !topk_three_pass_only()) ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c, a.T, 1);

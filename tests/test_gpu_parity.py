@@ -264,3 +264,47 @@ def test_empty_selection_row(lib):
     lib.sparse_mla_fwd(sa.batch, sa.layers[0], idx, spec.topk, out, lse, sa.workspace)
     assert lib.check_device_error() == lib.DSA_OK
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+@pytest.mark.parametrize("n,k,kind,cap", [
+    (32768, 2048, "normal", 0), (32768, 2048, "ties_top", 0), (131072, 2048, "normal", 0),
+    (1048576, 2048, "normal", 0), (300000, 2048, "ties", 0), (9000, 2048, "normal", 1),
+    (40000, 512, "normal", 0), (200000, 1024, "narrow", 0), (50000, 2048, "narrow", 4)])
+def test_topk_candidate_and_three_pass_paths_agree(lib, n, k, kind, cap):
+    # the candidate path (first digit across the cluster, the rest in one block)
+    # and the three-pass path must both give the oracle's selection
+    g = torch.Generator().manual_seed(3 * n + k)
+    T = 4
+    if kind == "normal":
+        s = torch.randn((T, n), generator=g)
+    elif kind == "ties":
+        s = torch.randint(-40, 41, (T, n), generator=g).float()
+    elif kind == "narrow":   # many keys in the threshold's first-digit bin
+        s = 1.0 + torch.rand((T, n), generator=g) * 1e-3
+    else:
+        s = torch.zeros((T, n))
+        s[:, torch.randperm(n, generator=g)[:300]] = 1.0
+    ld = (n + 3) // 4 * 4
+    scores = torch.zeros((T, ld), dtype=torch.float32)
+    scores[:, :n] = s
+    scores = scores.cuda()
+    cu = torch.arange(T + 1, dtype=torch.int32, device="cuda")
+    lens = torch.full((T,), n, dtype=torch.int32, device="cuda")
+    batch = lib.make_batch(cu, lens, T, n, 1)
+    ws = torch.empty(lib.workspace_size(batch, k), dtype=torch.uint8, device="cuda")
+    got = {}
+    lib.selftest_topk_max_cluster(cap)
+    try:
+        for cand in (True, False):
+            idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+            lib.selftest_topk_path(cand)
+            lib.topk(batch, scores, k, idx, ws)
+            assert lib.check_device_error() == lib.DSA_OK
+            got[cand] = idx.cpu()
+    finally:
+        lib.selftest_topk_path(True)
+        lib.selftest_topk_max_cluster(0)
+    assert torch.equal(got[True], got[False])
+    for t in range(T):
+        ref = oracle.topk_select(s[t].double().numpy(), k)
+        assert np.array_equal(sel_of(got[True][t].numpy()), ref), f"row {t}"
