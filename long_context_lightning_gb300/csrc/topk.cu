@@ -52,6 +52,7 @@ struct TopkParams {
   int32_t k;
   int32_t T;
   int32_t cache_keys;  // per-block key cache capacity (0: no cache)
+  int32_t cache_half;  // the cache holds the top 16 bits of each key (chunks up to twice as long)
   const int32_t* q_n;
   int* err;
   int32_t plan_early;  // the plan was written two or more grids back
@@ -113,12 +114,12 @@ __device__ __forceinline__ void block_select_digit(const uint32_t* h, int nb, ui
 }
 
 template <class Keys4>
-__device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hist, uint2* cand, bool cached, Keys4 keys4,
+__device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hist, uint2* cand, bool cached, bool half,
+                                               const uint16_t* cache16, Keys4 keys4,
                                             int len, int c0, uint32_t d0, uint32_t rem0, uint32_t own_above,
                                             uint32_t crank, uint32_t csize, int32_t* out, int* w_a, int* w_b,
                                             int* w_c, int* w_d, uint32_t* s_cand_n, uint32_t (*s_seg)[2],
                                             uint32_t* s_cbase, uint32_t* s_digit, uint32_t* s_rem) {
-  (void)cached;
   const int k = p.k;
   // (1) this block's candidates: its keys whose first digit is d0 or above, in position order
   const uint32_t mine = own_above + hist[d0];
@@ -128,33 +129,133 @@ __device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hi
     st_dsmem_u32(dsmem_addr(smem_u32(&s_seg[crank][0]), 0), base);
     st_dsmem_u32(dsmem_addr(smem_u32(&s_seg[crank][1]), 0), mine);
   }
-  const int R = ((len + kThreads - 1) / kThreads + 3) & ~3;
-  const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
-  int cnt = 0;
-  for (int i = r0; i < r1; i += 4) {
-    uint32_t kk[4];
-    keys4(i, kk);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) cnt += (i + j < r1) && (kk[j] >> 21) >= d0;
-  }
-  int total;
-  const int before = block_scan(cnt, w_a, w_b, &total);  // also orders s_cbase before its use
-  uint32_t slot = *s_cbase + (uint32_t)before;
   const uint32_t cand0 = dsmem_addr(smem_u32(cand), 0);
-  for (int i = r0; i < r1; i += 4) {
-    uint32_t kk[4];
-    keys4(i, kk);
+  if (cached) {
+    // thread t owns a contiguous run of the cached chunk
+    const int R = ((len + kThreads - 1) / kThreads + 3) & ~3;
+    const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
+    int cnt = 0;
+    for (int i = r0; i < r1; i += 4) {
+      uint32_t kk[4];
+      keys4(i, kk);
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if ((i + j < r1) && (kk[j] >> 21) >= d0) {
-        st_dsmem_v2_u32(cand0 + slot * 8u, kk[j], (uint32_t)(c0 + i + j));
-        ++slot;
+      for (int j = 0; j < 4; ++j) cnt += (i + j < r1) && (kk[j] >> 21) >= d0;
+    }
+    int total;
+    const int before = block_scan(cnt, w_a, w_b, &total);  // also orders s_cbase before its use
+    uint32_t slot = *s_cbase + (uint32_t)before;
+    for (int i = r0; i < r1; i += 4) {
+      uint32_t kk[4];
+      keys4(i, kk);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((i + j < r1) && (kk[j] >> 21) >= d0) {
+          st_dsmem_v2_u32(cand0 + slot * 8u, kk[j], (uint32_t)(c0 + i + j));
+          ++slot;
+        }
+    }
+  } else if (half) {
+    // thread t owns a contiguous run of the cached key tops (eight per
+    // 16-byte read); a candidate's full key is read back from global memory
+    const float* row = p.scores + (int64_t)blockIdx.y * p.ld_scores;
+    const int R = ((len + kThreads - 1) / kThreads + 7) & ~7;
+    const int r0 = min(len, (int)threadIdx.x * R), r1 = min(len, r0 + R);
+    int cnt = 0;
+    for (int i = r0; i < r1; i += 8) {
+      const uint4 q = *reinterpret_cast<const uint4*>(cache16 + i);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cnt += (i + j < r1) && (((w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) >> 5) >= d0;
+    }
+    int total;
+    const int before = block_scan(cnt, w_a, w_b, &total);  // also orders s_cbase before its use
+    uint32_t slot = *s_cbase + (uint32_t)before;
+    for (int i = r0; i < r1; i += 8) {
+      const uint4 q = *reinterpret_cast<const uint4*>(cache16 + i);
+      const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+      uint32_t cm = 0;  // which of the eight are candidates
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        cm |= (uint32_t)((i + j < r1) && (((w4[j >> 1] >> (16 * (j & 1))) & 0xFFFFu) >> 5) >= d0) << j;
+      if (cm) {
+        float f[8];  // the candidates' full scores, loads in flight together
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = ((cm >> j) & 1u) ? row[c0 + i + j] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if ((cm >> j) & 1u) {
+            st_dsmem_v2_u32(cand0 + slot * 8u, ordered_key(f[j]), (uint32_t)(c0 + i + j));
+            ++slot;
+          }
       }
+    }
+  } else {
+    // the chunk is read from global memory: warp w owns the contiguous span
+    // [w S, w S + S) (S a multiple of 512), read 512 keys at a time (four
+    // 16-byte loads in flight per lane); a counting pass, one scan of the warps'
+    // counts, then a writing pass that places each 128-key step with a warp scan
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int S = ((len + kWarps * 512 - 1) / (kWarps * 512)) * 512;
+    const int s0 = min(len, warp * S), s1 = min(len, s0 + S);
+    auto load4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4), 0 past the span
+      if (i + 3 < s1) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(p.scores + (int64_t)blockIdx.y * p.ld_scores + c0 + i));
+        kk[0] = ordered_key(f.x); kk[1] = ordered_key(f.y); kk[2] = ordered_key(f.z); kk[3] = ordered_key(f.w);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          kk[j] = (i + j < s1) ? ordered_key(p.scores[(int64_t)blockIdx.y * p.ld_scores + c0 + i + j]) : 0u;
+      }
+    };
+    int cnt = 0;
+    for (int i0 = s0; i0 < s1; i0 += 512) {
+      uint32_t kk[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load4(i0 + u * 128 + lane * 4, kk + 4 * u);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) cnt += (i0 + (u >> 2) * 128 + lane * 4 + (u & 3) < s1) && (kk[u] >> 21) >= d0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    int total;
+    const int before = block_scan(lane == 0 ? cnt : 0, w_a, w_b, &total);  // lane 0 carries its warp's count
+    uint32_t slot = *s_cbase + (uint32_t)__shfl_sync(0xffffffffu, before, 0);
+    for (int i0 = s0; i0 < s1; i0 += 512) {
+      uint32_t kk[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) load4(i0 + u * 128 + lane * 4, kk + 4 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * 128 + lane * 4;
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) c += (i + j < s1) && (kk[4 * u + j] >> 21) >= d0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        uint32_t q = slot + (uint32_t)(incl - c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((i + j < s1) && (kk[4 * u + j] >> 21) >= d0) {
+            st_dsmem_v2_u32(cand0 + q * 8u, kk[4 * u + j], (uint32_t)(c0 + i + j));
+            ++q;
+          }
+        slot += (uint32_t)__shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
   }
   cluster_sync();  // every block's candidates are in the first block; no one reads a peer's memory after this
   if (crank != 0) return;
 
   // (2) the first block: the last two digits among the candidates of bin d0
+  __shared__ uint32_t s_lo[kMaxCluster + 1];  // logical start of each block's segment (block-rank order)
+  if (threadIdx.x == 0) {
+    s_lo[0] = 0;
+    for (int r = 0; r < kMaxCluster; ++r) s_lo[r + 1] = s_lo[r] + ((uint32_t)r < csize ? s_seg[r][1] : 0u);
+  }
   const int n_c = (int)*s_cand_n;
   uint32_t* h1 = hist + kBins;
   uint32_t* h2 = hist + 2 * kBins;
@@ -175,27 +276,34 @@ __device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hi
   const uint32_t thr = (pre << 10) | *s_digit;  // the k-th largest key
   const int take = (int)*s_rem;                 // keys equal to it that are selected (lowest positions first)
 
-  // (3) ordered write: segments in block-rank order, each in position order
-  int out_pos = 0, eq_taken = 0;
-  for (uint32_t r = 0; r < csize; ++r) {
-    const int sb = (int)s_seg[r][0], sc = (int)s_seg[r][1];
-    const int Rs = (sc + kThreads - 1) / kThreads;
-    const int a0 = min(sc, (int)threadIdx.x * Rs), a1 = min(sc, a0 + Rs);
-    int gt = 0, eq = 0;
-    for (int i = a0; i < a1; ++i) {
-      const uint32_t key = cand[sb + i].x;
+  // (3) ordered write in one pass.  Logical candidate order = the segments in
+  // block-rank order, each in position order; thread t owns a contiguous run
+  // of it.  One scan of packed (above, equal) counts (both < 2^16) places
+  // every thread's first selection; equal keys go to the lowest positions.
+  auto phys = [&](int L, int& r) {  // physical slot of logical index L; r is the segment, advanced as L grows
+    while ((uint32_t)L >= s_lo[r + 1]) ++r;
+    return (int)s_seg[r][0] + L - (int)s_lo[r];
+  };
+  const int Rs = (n_c + kThreads - 1) / kThreads;
+  const int a0 = min(n_c, (int)threadIdx.x * Rs), a1 = min(n_c, a0 + Rs);
+  int gt = 0, eq = 0;
+  {
+    int r = 0;
+    for (int L = a0; L < a1; ++L) {
+      const uint32_t key = cand[phys(L, r)].x;
       gt += key > thr;
       eq += key == thr;
     }
-    int gt_tot, eq_tot;
-    const int gt_before = block_scan(gt, w_a, w_b, &gt_tot);
-    const int eq_before = block_scan(eq, w_c, w_d, &eq_tot);
-    const int left = take - eq_taken;
-    const int allow = max(0, min(eq, left - eq_before));
-    int pos = out_pos + gt_before + min(eq_before, max(left, 0));
-    int eq_seen = 0;
-    for (int i = a0; i < a1; ++i) {
-      const uint2 c = cand[sb + i];
+  }
+  int packed_tot;
+  const int packed_before = block_scan(gt | (eq << 16), w_a, w_b, &packed_tot);
+  const int gt_before = packed_before & 0xFFFF, eq_before = packed_before >> 16;
+  const int allow = max(0, min(eq, take - eq_before));
+  int pos = gt_before + min(eq_before, take);
+  {
+    int r = 0, eq_seen = 0;
+    for (int L = a0; L < a1; ++L) {
+      const uint2 c = cand[phys(L, r)];
       const bool e = c.x == thr;
       if (c.x > thr || (e && eq_seen < allow)) {
         if (pos < k) out[pos] = (int32_t)c.y;
@@ -203,28 +311,32 @@ __device__ __forceinline__ void candidate_path(const TopkParams& p, uint32_t* hi
       }
       eq_seen += e;
     }
-    const int eq_used = min(eq_tot, max(left, 0));
-    out_pos += gt_tot + eq_used;
-    eq_taken += eq_used;
   }
+  (void)w_c;
+  (void)w_d;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* hist = sm;                    // [3][kBins] this block's digit histograms
-  uint32_t* tot = sm + 3 * kBins;         // [kBins] cluster-summed histogram of the current digit
-  uint32_t* cache = sm + 4 * kBins;       // [cache_keys]
-  uint2* cand = reinterpret_cast<uint2*>(cache + p.cache_keys);  // [kCand] (key, position), first block only
+  uint32_t* cache = sm + 3 * kBins;       // [cache_keys] keys, or [cache_keys] 16-bit key tops
+  uint16_t* cache16 = reinterpret_cast<uint16_t*>(cache);
+  uint2* cand = reinterpret_cast<uint2*>(cache + (p.cache_half ? p.cache_keys / 2 : p.cache_keys));  // [kCand]
   __shared__ int w_gt[kWarps], w_eq[kWarps], w_eqb[kWarps], w_selb[kWarps];
   __shared__ uint32_t s_digit, s_rem, s_local_above;
   __shared__ uint32_t s_xch[2];           // this block's (keys above threshold, keys equal to it)
   __shared__ uint32_t s_cand_n;           // first block: candidate slots reserved so far
   __shared__ uint32_t s_seg[kMaxCluster][2];  // first block: (first slot, count) of each block's candidates
   __shared__ uint32_t s_cbase;
+  __shared__ uint32_t coarse[3][64];      // per digit: this block's sums of 32 consecutive bins
+  __shared__ uint32_t s_tot_d;            // the cluster's count of the chosen digit's bin
 
   const int t = blockIdx.y;
   const uint32_t crank = cluster_ctarank();
   const uint32_t csize = cluster_nctarank();
+  // block-local set-up needs nothing from the previous grids: done before waiting for them
+  for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) hist[i] = 0;
+  if (threadIdx.x == 0) s_cand_n = 0;  // before the first cluster barrier, so before any peer's reservation
   int n = p.plan_early ? __ldcg(p.q_n + t) : 0;
   pdl_wait();  // scores and plan of the previous grids are complete from here on
   pdl_trigger();
@@ -242,11 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
   const int per = ((n + csize - 1) / csize + 3) & ~3;
   const int c0 = min(n, (int)crank * per), c1 = min(n, c0 + per);
   const int len = c1 - c0;
-  const bool cached = len <= p.cache_keys;
+  const bool cached = !p.cache_half && len <= p.cache_keys;
+  const bool half = p.cache_half && len <= p.cache_keys;
   const float* row = p.scores + (int64_t)t * p.ld_scores;
 
-  for (int i = threadIdx.x; i < 3 * kBins; i += kThreads) hist[i] = 0;
-  if (threadIdx.x == 0) s_cand_n = 0;  // before the first cluster barrier, so before any peer's reservation
   __syncthreads();
   auto keys4 = [&](int i, uint32_t* kk) {  // keys i..i+3 of the chunk (i a multiple of 4, i < len)
     if (cached) {
@@ -297,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
             const bool in = c0 + i + j < c1;
             const uint32_t key = ordered_key(v[4 * u + j]);
             if (cached && in) cache[i + j] = key;
+            if (half && in) cache16[i + j] = (uint16_t)(key >> 16);
             hist_add(h, key >> sh, in);
           }
         }
@@ -309,76 +421,84 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
         for (int j = 0; j < 4; ++j) hist_add(h, (kk[j] >> sh) & msk, i + j < len && (kk[j] >> psh) == prefix);
       }
     }
-    cluster_sync();  // every block's histogram of this digit is complete
-    // ---- cluster-wide histogram and the digit holding the rem-th largest key.
-    // Thread t owns the bins just below those of thread t-1 (thread 0 the top
-    // ones); it sums them over the cluster, and one block scan of (cluster
-    // count, own count) pairs gives, at the chosen digit, both the keys above
-    // it in the cluster and this block's own keys above it.
+    // ---- coarse sums of this block's histogram: group g = bins [32 g, 32 g + 32)
     const int nb = (int)msk + 1;
-    const int bpt = nb / kThreads;  // 2 or 1 bins per thread
-    const int top = nb - 1 - (int)threadIdx.x * bpt;
-    int tot_mine = 0, own_mine = 0;
-    if (bpt == 2) {
-      // the thread's two bins are adjacent and 8-byte aligned: one remote load per peer
-      const int b0 = top - 1;
-      uint32_t s0 = h[b0], s1 = h[b0 + 1];
-      const uint32_t local = smem_u32(h + b0);
-      for (uint32_t r = 0; r < csize; ++r)
-        if (r != crank) {
-          const uint2 v = ld_dsmem_v2_u32(dsmem_addr(local, r));
-          s0 += v.x;
-          s1 += v.y;
-        }
-      tot[b0] = s0;
-      tot[b0 + 1] = s1;
-      tot_mine = (int)(s0 + s1);
-      own_mine = (int)(h[b0] + h[b0 + 1]);
-    } else {
-      uint32_t sum = h[top];
-      const uint32_t local = smem_u32(h + top);
-      for (uint32_t r = 0; r < csize; ++r)
-        if (r != crank) sum += ld_dsmem_u32(dsmem_addr(local, r));
-      tot[top] = sum;
-      tot_mine = (int)sum;
-      own_mine = (int)h[top];
+    const int ng = nb / 32;  // 64 or 32 groups
+    __syncthreads();         // every thread's histogram adds are done
+    for (int g = warp; g < ng; g += kWarps) {
+      uint32_t v = h[g * 32 + lane];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) coarse[pass][g] = v;
     }
-    const int tot_ex = warp_excl_scan(tot_mine), own_ex = warp_excl_scan(own_mine);
-    if (lane == 31) {
-      w_gt[warp] = tot_ex + tot_mine;  // warp totals (reusing the write-phase scratch)
-      w_eq[warp] = own_ex + own_mine;
-    }
-    __syncthreads();
+    cluster_sync();  // every block's histogram and coarse sums of this digit are complete
+    // ---- the digit holding the rem-th largest key (warp 0): the cluster's
+    // coarse sums, top group first, pick a group; the cluster's counts of its 32
+    // bins pick the digit.  Exclusive scans of the cluster counts and of this
+    // block's own counts give, at the pick, the keys above it in the cluster
+    // and this block's own keys above it.
     if (warp == 0) {
-      const int a_t = w_gt[lane], a_o = w_eq[lane];
-      w_eqb[lane] = warp_excl_scan(a_t);
-      w_selb[lane] = warp_excl_scan(a_o);
-    }
-    __syncthreads();
-    {
-      int acc_t = w_eqb[warp] + tot_ex, acc_o = w_selb[warp] + own_ex;  // keys above this thread's bins
-      if ((uint32_t)acc_t < rem && rem <= (uint32_t)(acc_t + tot_mine)) {
-        for (int j = 0; j < bpt; ++j) {
-          const int bin = top - j;
-          const int cnt = (int)tot[bin];
-          if ((uint32_t)(acc_t + cnt) >= rem) {
-            s_digit = bin;
-            s_rem = rem - acc_t;
-            s_local_above = acc_o;
-            break;
+      auto peer_sum = [&](const uint32_t* v) -> uint32_t {  // over the other blocks, four loads in flight
+        const uint32_t local = smem_u32(v);
+        uint32_t sum = 0;
+        for (uint32_t rb = 0; rb < csize; rb += 4) {
+          uint32_t x[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t r = rb + j;
+            x[j] = (r < csize && r != crank) ? ld_dsmem_u32(dsmem_addr(local, r)) : 0u;
           }
-          acc_t += cnt;
-          acc_o += (int)h[bin];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) sum += x[j];
         }
+        return sum;
+      };
+      const int gpl = ng / 32;  // groups per lane, lane 0 the top ones
+      uint32_t c_all[2] = {0u, 0u}, c_own[2] = {0u, 0u};
+      for (int j = 0; j < gpl; ++j) {
+        const int g = ng - 1 - lane * gpl - j;
+        c_own[j] = coarse[pass][g];
+        c_all[j] = c_own[j] + peer_sum(&coarse[pass][g]);
+      }
+      const uint32_t lane_all = c_all[0] + c_all[1], lane_own = c_own[0] + c_own[1];
+      const uint32_t ex_all = (uint32_t)warp_excl_scan((int)lane_all), ex_own = (uint32_t)warp_excl_scan((int)lane_own);
+      const unsigned m = __ballot_sync(0xffffffffu, ex_all < rem && rem <= ex_all + lane_all);
+      const int src = m ? __ffs(m) - 1 : 31;
+      int G = 0;
+      uint32_t above_all = 0, above_own = 0;
+      if (lane == src) {
+        uint32_t acc = ex_all, acco = ex_own;
+        for (int j = 0; j < gpl; ++j) {
+          G = ng - 1 - lane * gpl - j;
+          if (acc + c_all[j] >= rem) break;
+          acc += c_all[j];
+          acco += c_own[j];
+        }
+        above_all = acc;
+        above_own = acco;
+      }
+      G = __shfl_sync(0xffffffffu, G, src);
+      above_all = __shfl_sync(0xffffffffu, above_all, src);
+      above_own = __shfl_sync(0xffffffffu, above_own, src);
+      const uint32_t rem_g = rem - above_all;
+      const int b = G * 32 + 31 - lane;  // lane 0 the group's top bin
+      const uint32_t f_own = h[b], f_all = f_own + peer_sum(&h[b]);
+      const uint32_t fx_all = (uint32_t)warp_excl_scan((int)f_all), fx_own = (uint32_t)warp_excl_scan((int)f_own);
+      const unsigned fm = __ballot_sync(0xffffffffu, fx_all < rem_g && rem_g <= fx_all + f_all);
+      if (lane == (fm ? __ffs(fm) - 1 : 31)) {
+        s_digit = (uint32_t)b;
+        s_rem = rem_g - fx_all;
+        s_local_above = above_own + fx_own;
+        s_tot_d = f_all;
       }
     }
     __syncthreads();
     local_greater += s_local_above;
     prefix = (prefix << bits) | s_digit;
     rem = s_rem;
-    if (pass == 0 && p.cand && (uint32_t)k - rem + tot[prefix] <= (uint32_t)kCand) {
-      candidate_path(p, hist, cand, cached, keys4, len, c0, prefix, rem, local_greater, crank, csize, out, w_gt,
-                     w_eq, w_selb, w_eqb, &s_cand_n, s_seg, &s_cbase, &s_digit, &s_rem);
+    if (pass == 0 && p.cand && (uint32_t)k - rem + s_tot_d <= (uint32_t)kCand) {
+      candidate_path(p, hist, cand, cached, half, cache16, keys4, len, c0, prefix, rem, local_greater, crank, csize,
+                     out, w_gt, w_eq, w_selb, w_eqb, &s_cand_n, s_seg, &s_cbase, &s_digit, &s_rem);
       return;
     }
     __syncthreads();  // the next pass rewrites s_digit, s_rem, s_local_above and the scratch
@@ -488,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) topk_kernel(TopkParams p) {
 
 cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
-  const int probe_smem = (4 * kBins + kMaxCacheKeys + 2 * kCand) * 4;
+  const int probe_smem = (3 * kBins + kMaxCacheKeys + 2 * kCand) * 4;
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, probe_smem);
   if (e != cudaSuccess) return e;
   int max_cluster = max_cluster_for(reinterpret_cast<const void*>(topk_kernel), kThreads, probe_smem,
@@ -500,9 +620,12 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   int c = 1;
   while (c < max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
   while (c < max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
-  const int per = (((a.max_n + c - 1) / c) + 3) & ~3;
-  const int cache_keys = per <= kMaxCacheKeys ? per : 0;
-  const size_t smem = (size_t)(4 * kBins + cache_keys + 2 * kCand) * 4;
+  const int per = (((a.max_n + c - 1) / c) + 7) & ~7;
+  // the cache holds whole keys, or the top 16 bits of each key of a chunk up to twice as long
+  const int cache_half = per > kMaxCacheKeys && per <= 2 * kMaxCacheKeys;
+  const int cache_keys = per <= 2 * kMaxCacheKeys ? per : 0;
+  const size_t cache_words = cache_half ? (size_t)cache_keys / 2 : (size_t)cache_keys;
+  const size_t smem = (3 * kBins + cache_words + 2 * kCand) * 4;
   e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
 
@@ -514,6 +637,7 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   p.k = a.k;
   p.T = a.T;
   p.cache_keys = cache_keys;
+  p.cache_half = cache_half;
   p.q_n = a.q_n;
   p.err = a.err;
   p.plan_early = a.plan_early ? 1 : 0;
