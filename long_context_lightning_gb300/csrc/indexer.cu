@@ -13,12 +13,16 @@
 // cross-thread reduction, and writes one fp32 score per (query, key).  The
 // per-head logits never leave the SM.
 //
-// Warp roles (192 threads, one block per SM, persistent over the work list):
+// Warp roles (one block per SM, persistent over the work list):
 //   warp 0      TMA producer: key tiles into a ring of stages, the group's
 //               indexer queries into the B buffer
 //   warp 1      TMEM owner and MMA issuer (one elected thread)
-//   warps 2..5  epilogue, one per TMEM lane quadrant; two accumulators in
-//               TMEM so the epilogue of item i overlaps the MMA of item i+1
+//   warps 2..   epilogue: four warps (one per TMEM lane quadrant) for
+//               one-query groups, eight for four-query groups (two per
+//               quadrant, each owning two of the queries, so the per-key
+//               ReLU / weight / head-sum work of a tile is split two ways);
+//               two accumulators in TMEM so the epilogue of item i overlaps
+//               the MMA of item i+1
 #include <algorithm>
 
 #include "internal.cuh"
@@ -38,7 +42,10 @@ struct IdxCfg {
   static constexpr int STAGES_FIT = (SMEM_BUDGET - BSLOTS * B_BYTES - 4096) / A_BYTES;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr int TMEM_COLS = (2 * N <= 32) ? 32 : (2 * N <= 64) ? 64 : (2 * N <= 128) ? 128 : (2 * N <= 256) ? 256 : 512;
-  static constexpr int THREADS = 192;
+  static constexpr int EPI_WARPS = (G > 1) ? 8 : 4;  // epilogue warps
+  static constexpr int EPI = 32 * EPI_WARPS;
+  static constexpr int QH = G * 4 / EPI_WARPS;         // queries per epilogue warp
+  static constexpr int THREADS = 64 + EPI;
   // shared memory map (offsets from a 1024-aligned base)
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -82,7 +89,7 @@ __device__ __forceinline__ int find_group_warp(const int32_t* start, int n_group
 }
 
 template <int KB, int NH, int G>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(IdxCfg<KB, NH, G>::THREADS, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
                    IdxParams p) {
   using C = IdxCfg<KB, NH, G>;
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(bar_acc_full(a), 1);
-      mbar_init(bar_acc_empty(a), 128);
+      mbar_init(bar_acc_empty(a), C::EPI);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -270,14 +277,15 @@ __global__ void __launch_bounds__(192, 1)
     // ----------------------------------------------------------- epilogue
     const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
     const int row = quad * 32 + lane;    // key within the tile
-    const int et = threadIdx.x - 64;     // 0..127
+    const int et = threadIdx.x - 64;     // 0 .. EPI-1
+    const int qh0 = ((warp - 2) >> 2) * C::QH;  // this warp's first query of the group
     int acc = 0;
     uint32_t acc_phase = 0;
     bool bad = (w0 >= w1);
     int g = g_first;
     int g_next = bad ? 0 : __ldg(gstart + g + 1);
     int4 gi = make_int4(0, 0, 0, 0);
-    int qn[G];
+    int qn[C::QH];
     for (int item = w0; item < w1; ++item) {
       bool new_group = (item == w0);
       while (item >= g_next) {
@@ -287,16 +295,16 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (new_group) {
         gi = p.plan.g_info[g];
-        named_bar_sync(1, 128);  // previous group's readers of w_s are done
-        for (int i = et; i < G * NH; i += 128) {
+        named_bar_sync(1, C::EPI);  // previous group's readers of w_s are done
+        for (int i = et; i < G * NH; i += C::EPI) {
           const int q = i / NH, h = i % NH;
           float v = 0.f;
           if (q < gi.z && h < p.H) v = __ldg(p.w + (int64_t)(gi.y + q) * p.H + h);
           w_s[i] = v;
         }
 #pragma unroll
-        for (int q = 0; q < G; ++q) qn[q] = (q < gi.z) ? p.plan.q_n[gi.y + q] : 0;
-        named_bar_sync(1, 128);
+        for (int qq = 0; qq < C::QH; ++qq) qn[qq] = (qh0 + qq < gi.z) ? p.plan.q_n[gi.y + qh0 + qq] : 0;
+        named_bar_sync(1, C::EPI);
       }
       const int kt = item - __ldg(gstart + g);
       if (!bad && !mbar_wait(bar_acc_full(acc), acc_phase, abort_flag, p.err)) bad = true;
@@ -304,16 +312,19 @@ __global__ void __launch_bounds__(192, 1)
       const int64_t s = (int64_t)kt * 128 + row;
       const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + acc * C::N;
 #pragma unroll
-      for (int q = 0; q < G; ++q) {
-        float score = 0.f;
+      for (int qq = 0; qq < C::QH; ++qq) {
+        const int q = qh0 + qq;
         uint32_t r[NH];  // all head columns of this query, one wait
 #pragma unroll
         for (int hc = 0; hc < NH / 16; ++hc)
           tmem_ld16(tbase + q * NH + hc * 16, *reinterpret_cast<uint32_t(*)[16]>(r + hc * 16));
         tmem_wait_ld();
+        float part[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains over the heads
 #pragma unroll
-        for (int j = 0; j < NH; ++j) score = fmaf(w_s[q * NH + j], fmaxf(__uint_as_float(r[j]), 0.f), score);
-        if (!bad && q < gi.z && s < qn[q]) p.scores[(int64_t)(gi.y + q) * p.ld + s] = score;
+        for (int j = 0; j < NH; ++j)
+          part[j & 3] = fmaf(w_s[q * NH + j], fmaxf(__uint_as_float(r[j]), 0.f), part[j & 3]);
+        const float score = (part[0] + part[1]) + (part[2] + part[3]);
+        if (!bad && q < gi.z && s < qn[qq]) p.scores[(int64_t)(gi.y + q) * p.ld + s] = score;
       }
       tc_fence_before();
       mbar_arrive(bar_acc_empty(acc));
