@@ -308,3 +308,37 @@ def test_topk_candidate_and_three_pass_paths_agree(lib, n, k, kind, cap):
     for t in range(T):
         ref = oracle.topk_select(s[t].double().numpy(), k)
         assert np.array_equal(sel_of(got[True][t].numpy()), ref), f"row {t}"
+
+
+@pytest.mark.parametrize("cap", [0, 4])
+def test_topk_many_rows_mixed_paths(lib, cap):
+    # more rows than clusters fit on the GPU at once: each cluster takes a share
+    # of the rows, alternating dense rows, candidate-path rows and rows whose
+    # threshold bin is too large for the candidates (three-pass path)
+    g = torch.Generator().manual_seed(99 + cap)
+    T, k = 700, 512
+    lens = torch.randint(100, 40000, (T,), generator=g)
+    lens[::7] = torch.randint(10, k + 1, (len(lens[::7]),), generator=g)   # dense rows
+    n_max = int(lens.max())
+    ld = (n_max + 3) // 4 * 4
+    scores = torch.randn((T, ld), generator=g)
+    scores[1::5] = 2.0 + torch.rand((len(scores[1::5]), ld), generator=g) * 1e-4  # one huge threshold bin
+    scores[2::9] = torch.randint(-3, 4, (len(scores[2::9]), ld), generator=g).float()
+    cu = torch.arange(T + 1, dtype=torch.int32).cuda()
+    lens_d = lens.to(torch.int32).cuda()
+    batch = lib.make_batch(cu, lens_d, T, n_max, 1)
+    ws = torch.empty(lib.workspace_size(batch, k), dtype=torch.uint8, device="cuda")
+    idx = torch.full((T, k), -7, dtype=torch.int32, device="cuda")
+    lib.selftest_topk_max_cluster(cap)
+    try:
+        lib.topk(batch, scores.cuda(), k, idx, ws)
+        assert lib.check_device_error() == lib.DSA_OK
+    finally:
+        lib.selftest_topk_max_cluster(0)
+    got = idx.cpu().numpy()
+    for t in range(T):
+        n = int(lens[t])
+        ref = oracle.topk_select(scores[t, :n].double().numpy(), k)
+        sel = sel_of(got[t])
+        assert np.array_equal(sel, ref), f"row {t} (n={n})"
+        assert np.all(got[t][len(sel):] == -1)
