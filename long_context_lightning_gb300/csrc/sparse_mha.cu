@@ -25,9 +25,12 @@
 //            of two TMEM buffers, online softmax in fp32 over the selected
 //            keys only (a per-row reference that moves when a score passes it
 //            by more than 2^8, so O is rescaled in TMEM only then), P in bf16
-//            to shared memory, O += P V (M = 128, N = 256, K = 64) in TMEM.
-//            Warp 0 streams Q once and K/V tiles through two stages with TMA,
-//            warp 1 issues the MMAs, warps 2-5 own one query row per thread.
+//            to one of two shared buffers, O += P V (M = 128, N = 256, K = 64)
+//            in TMEM.  Warp 0 streams Q once and K/V tiles through two stages
+//            with TMA, warp 1 issues the MMAs, warps 2-9 do the softmax: two
+//            threads per query row, both finding the row maximum over the
+//            tile's 64 keys, each exponentiating 32 of them and owning 128 of
+//            the row's output columns.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -212,17 +215,17 @@ __global__ void __launch_bounds__(256) mha_mask_kernel(MaskParams p) {
 // -------------------------------------------------------------- attend ---
 
 struct AttCfg {
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 64 + 256;               // producer, MMA issuer, eight softmax warps
   static constexpr int Q_BYTES = 128 * kHead * 2;        // 64 KB: 4 blocks [128 x 64]
   static constexpr int K_BYTES = 64 * kHead * 2;         // 32 KB: 4 blocks [64 x 64]
   static constexpr int V_BYTES = 64 * kHead * 2;         // 32 KB: 4 value blocks [64 keys x 64]
   static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int P_BYTES = 128 * 64 * 2;           // 16 KB: [128 queries x 64 keys]
+  static constexpr int P_BYTES = 128 * 64 * 2;           // 16 KB: [128 queries x 64 keys], two buffers
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = OFF_Q + Q_BYTES;
   static constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  static constexpr int N_BARS = 12;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int N_BARS = 18;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int TMEM_COLS = 512;                  // O: 256 columns, S: two buffers of 64
@@ -254,13 +257,15 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const uint32_t q_full = smem_u32(bars + 0);
-  auto kv_full = [&](int s) { return smem_u32(bars + 1 + s); };
-  auto kv_empty = [&](int s) { return smem_u32(bars + 3 + s); };
-  auto s_full = [&](int u) { return smem_u32(bars + 5 + u); };
-  auto s_free = [&](int u) { return smem_u32(bars + 7 + u); };
-  const uint32_t p_full = smem_u32(bars + 9);
-  const uint32_t pv_done = smem_u32(bars + 10);
-  const uint32_t drain = smem_u32(bars + 11);
+  auto k_full = [&](int s) { return smem_u32(bars + 1 + s); };
+  auto k_empty = [&](int s) { return smem_u32(bars + 3 + s); };
+  auto v_full = [&](int s) { return smem_u32(bars + 5 + s); };
+  auto v_empty = [&](int s) { return smem_u32(bars + 7 + s); };
+  auto s_full = [&](int u) { return smem_u32(bars + 9 + u); };
+  auto s_free = [&](int u) { return smem_u32(bars + 11 + u); };
+  auto p_full = [&](int u) { return smem_u32(bars + 13 + u); };
+  auto pv_done = [&](int u) { return smem_u32(bars + 15 + u); };
+  const uint32_t drain = smem_u32(bars + 17);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_wait();  // the plan and the masks are complete from here on
@@ -274,13 +279,15 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
-      mbar_init(s_free(s), 128);
+      mbar_init(s_free(s), 256);
+      mbar_init(p_full(s), 256);
+      mbar_init(pv_done(s), 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -309,36 +316,64 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
     if (lane == 0 && n_kt > 0) {
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int kb = 0; kb < 4; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 16384, &tm_q, q_full, kb * 64, h, q0);
-      int issued = 0;
-      for (int j = 0; j < n_kt; ++j) {
+      // keys and values have stages of their own: a key stage is free once
+      // its S = Q K^T is done, a value stage only after its P.V, so keys are
+      // loaded one tile ahead of values.  A 64-key tile is one 64-token page.
+      const int32_t* pt = p.kv.paged ? p.kv.page_table + (int64_t)b * p.kv.pt_stride : nullptr;
+      const int64_t start = p.kv.paged ? 0 : __ldg(p.kv.seq_start + b);
+      int64_t row_of[2] = {0, 0};
+      bool valid_of[2] = {false, false};
+      int issued_k = 0, issued_v = 0;
+      auto issue_k = [&](int j) -> bool {
         const int s = j & 1;
-        if (j >= 2 && !mbar_wait(kv_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) break;
         int64_t row0;
-        bool valid = true;
-        if (p.kv.paged) {  // a 64-key tile is one 64-token page
-          const int64_t phys = __ldg(p.kv.page_table + (int64_t)b * p.kv.pt_stride + j);
+        bool valid;
+        if (p.kv.paged) {
+          const int64_t phys = __ldg(pt + j);
           valid = phys >= 0 && (phys + 1) * 64 <= p.kv.num_rows;
           row0 = phys * 64;
         } else {
-          row0 = __ldg(p.kv.seq_start + b) + (int64_t)j * 64;
+          row0 = start + (int64_t)j * 64;
           valid = row0 >= 0 && row0 < p.kv.num_rows;
         }
+        row_of[s] = row0;
+        valid_of[s] = valid;
+        if (j >= 2 && !mbar_wait(k_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
         const uint32_t dst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
         if (valid) {
-          mbar_arrive_expect_tx(kv_full(s), C::STAGE_BYTES);
-          for (int kb = 0; kb < 4; ++kb) {
-            tma_load_3d(dst + kb * 8192, &tm_k, kv_full(s), kb * 64, h, (int32_t)row0);
-            tma_load_3d(dst + C::K_BYTES + kb * 8192, &tm_v, kv_full(s), kb * 64, h, (int32_t)row0);
-          }
+          mbar_arrive_expect_tx(k_full(s), C::K_BYTES);
+          for (int kb = 0; kb < 4; ++kb) tma_load_3d(dst + kb * 8192, &tm_k, k_full(s), kb * 64, h, (int32_t)row0);
         } else {
           atomicOr(p.err, DEV_ERR_BAD_INDEX);
-          mbar_arrive(kv_full(s));  // nothing loaded: the stage keeps earlier (finite) contents
+          mbar_arrive(k_full(s));  // nothing loaded: the stage keeps earlier (finite) contents
         }
-        ++issued;
+        ++issued_k;
+        return true;
+      };
+      auto issue_v = [&](int j) -> bool {
+        const int s = j & 1;
+        if (j >= 2 && !mbar_wait(v_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
+        const uint32_t dst = sbase + C::OFF_KV + s * C::STAGE_BYTES + C::K_BYTES;
+        if (valid_of[s]) {
+          mbar_arrive_expect_tx(v_full(s), C::V_BYTES);
+          for (int kb = 0; kb < 4; ++kb)
+            tma_load_3d(dst + kb * 8192, &tm_v, v_full(s), kb * 64, h, (int32_t)row_of[s]);
+        } else {
+          mbar_arrive(v_full(s));
+        }
+        ++issued_v;
+        return true;
+      };
+      if (issue_k(0)) {
+        for (int j = 0; j < n_kt; ++j) {
+          if (j + 1 < n_kt && !issue_k(j + 1)) break;
+          if (!issue_v(j)) break;
+        }
       }
       if (*abort_flag) {
         mbar_wait_drain(q_full, 0);
-        for (int j = std::max(0, issued - 2); j < issued; ++j) mbar_wait_drain(kv_full(j & 1), (j >> 1) & 1);
+        for (int j = std::max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_drain(k_full(j & 1), (j >> 1) & 1);
+        for (int j = std::max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_drain(v_full(j & 1), (j >> 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -347,11 +382,8 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       const uint32_t idesc_s = mma_idesc_bf16(128, 64, false, false);
       const uint32_t idesc_o = mma_idesc_bf16(128, kHead, false, true);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j) {
         const int u = j & 1;
-        if (!mbar_wait(kv_full(u), (j >> 1) & 1, abort_flag, p.err)) return false;
-        if (j >= 2 && !mbar_wait(s_free(u), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
-        tc_fence_after();
         const uint32_t kbase = sbase + C::OFF_KV + u * C::STAGE_BYTES;
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb)
@@ -359,37 +391,81 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16(tmem + C::S_COL + u * 64, smem_desc_sw128(sbase + C::OFF_Q + kb * 16384 + ks * 32, 16, 1024),
                      smem_desc_sw128(kbase + kb * 8192 + ks * 32, 16, 1024), idesc_s, (kb | ks) != 0);
+        mma_commit(k_empty(u));
         mma_commit(s_full(u));
-        return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; j < n_kt && ok; ++j) {
-        if (j + 1 < n_kt && !(ok = issue_s(j + 1))) break;
-        if (!(ok = mbar_wait(p_full, j & 1, abort_flag, p.err))) break;
-        tc_fence_after();
-        const uint32_t vbase = sbase + C::OFF_KV + (j & 1) * C::STAGE_BYTES + C::K_BYTES;
+      auto issue_pv = [&](int j) {
+        const int u = j & 1;
+        const uint32_t vbase = sbase + C::OFF_KV + u * C::STAGE_BYTES + C::K_BYTES;
+        const uint32_t pbase = sbase + C::OFF_P + u * C::P_BYTES;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem, smem_desc_sw128(sbase + C::OFF_P + ks * 32, 16, 1024),
+          mma_bf16(tmem, smem_desc_sw128(pbase + ks * 32, 16, 1024),
                    smem_desc_sw128(vbase + ks * 2048, 8192, 1024), idesc_o, (j | ks) != 0);
-        mma_commit(kv_empty(j & 1));
-        mma_commit(pv_done);
+        mma_commit(v_empty(u));
+        mma_commit(pv_done(u));
+      };
+      auto ready_s = [&](int j) {
+        const int u = j & 1;
+        return mbar_test_wait(k_full(u), (j >> 1) & 1) &&
+               (j < 2 || mbar_test_wait(s_free(u), ((j >> 1) - 1) & 1));
+      };
+      auto ready_pv = [&](int j) {
+        const int u = j & 1;
+        return mbar_test_wait(p_full(u), (j >> 1) & 1) && mbar_test_wait(v_full(u), (j >> 1) & 1);
+      };
+      if (ok && (ok = mbar_wait(k_full(0), 0, abort_flag, p.err))) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      // per tile: the next tile's S and this tile's P.V, whichever is ready first
+      for (int j = 0; j < n_kt && ok; ++j) {
+        bool need_s = j + 1 < n_kt, need_pv = true;
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t spin = 1; need_s || need_pv; ++spin) {
+          if (need_s && ready_s(j + 1)) {
+            tc_fence_after();
+            issue_s(j + 1);
+            need_s = false;
+          } else if (need_pv && ready_pv(j)) {
+            tc_fence_after();
+            issue_pv(j);
+            need_pv = false;
+          } else if ((spin & 31) == 0) {
+            if (*abort_flag) {
+              ok = false;
+              break;
+            }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+              *abort_flag = 1;
+              atomicOr(p.err, DEV_ERR_TIMEOUT);
+              ok = false;
+              break;
+            }
+          }
+        }
       }
       mma_commit(drain);  // every MMA of this thread done before TMEM is freed
       mbar_wait_drain(drain, 0);
     }
   } else {
-    // -------------------------------------------- softmax, one row per thread
+    // ------------------------------- softmax, two threads per query row
     const int qd = warp & 3;
+    const int hf = (warp - 2) >> 2;  // which half of the tile's keys / of the row's outputs
     const int row = qd * 32 + lane;
     const int t = q0 + row;
     const bool valid_q = row < cnt;
     const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
     const uint32_t* mrow = p.mask + (int64_t)(valid_q ? t : 0) * p.W;
-    float m_ref = neg_inf(), l = 0.f;
+    float m_ref = neg_inf(), l = 0.f;  // l: this thread's half of the row sum
     bool ok = true;
+    // the selection bits of a tile are loaded one tile ahead, so their latency
+    // hides behind the previous tile
+    uint2 bits_next = (valid_q && n_kt > 0) ? __ldg(reinterpret_cast<const uint2*>(mrow)) : make_uint2(0u, 0u);
     for (int j = 0; j < n_kt; ++j) {
       const int u = j & 1;
+      const uint2 bits = bits_next;
+      if (valid_q && j + 1 < n_kt) bits_next = __ldg(reinterpret_cast<const uint2*>(mrow + 2 * (j + 1)));
       if (!(ok = mbar_wait(s_full(u), (j >> 1) & 1, abort_flag, p.err))) break;
       tc_fence_after();
       uint32_t sv[64];
@@ -406,28 +482,33 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       }
       tc_fence_before();
       mbar_arrive(s_free(u));
-      const uint2 bits = valid_q ? *reinterpret_cast<const uint2*>(mrow + 2 * j) : make_uint2(0u, 0u);
-      float x[64];
+      // the maximum over all 64 keys (both threads of the row find the same),
+      // the exponentials for this thread's 32
       float mt = neg_inf();
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         const uint32_t bit = ((c < 32 ? bits.x : bits.y) >> (c & 31)) & 1u;
-        x[c] = bit ? __uint_as_float(sv[c]) * p.scale_log2 : neg_inf();
-        mt = fmaxf(mt, x[c]);
+        if (bit) mt = fmaxf(mt, __uint_as_float(sv[c]) * p.scale_log2);
       }
-      // the P buffer and O are the previous PV's until it completes
-      if (j > 0 && !(ok = mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.err))) break;
-      tc_fence_after();
+      const uint32_t mine = hf ? bits.y : bits.x;
+      float x[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        x[c] = ((mine >> c) & 1u) ? __uint_as_float(hf ? sv[32 + c] : sv[c]) * p.scale_log2 : neg_inf();
       // the reference moves when a score passes it by more than 2^8; O and l
       // follow it (TMEM loads and stores are warp-wide: a row that keeps its
-      // reference is scaled by 1)
+      // reference is scaled by 1).  Rescaling O needs the previous P.V done.
       const bool move = mt > m_ref + 8.f;
-      const bool need = move && j > 0 && l > 0.f;
+      // O holds something once any earlier key of the row was selected (the
+      // reference is finite then), whichever half of the tile it was in
+      const bool need = move && j > 0 && m_ref != neg_inf();
       const float f = need ? ex2_approx(m_ref - mt) : 1.f;
       const bool rescaled = __any_sync(0xffffffffu, need);
       if (rescaled) {
+        if (!(ok = mbar_wait(pv_done((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag, p.err))) break;
+        tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 0; c0 < kHead; c0 += 32) {
+        for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_base + c0, o);
           tmem_wait_ld();
@@ -438,10 +519,10 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       }
       l *= f;
       if (move) m_ref = mt;
+      uint32_t pk[16];
       float lsum = 0.f;
-      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
+      for (int c = 0; c < 32; c += 2) {
         const float p0 = x[c] == neg_inf() ? 0.f : ex2_approx(x[c] - m_ref);
         const float p1 = x[c + 1] == neg_inf() ? 0.f : ex2_approx(x[c + 1] - m_ref);
         const uint32_t w = pack_bf16x2(p0, p1);
@@ -449,21 +530,29 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
         pk[c >> 1] = w;
       }
       l += lsum;
-      const uint32_t prow = sbase + C::OFF_P + row * 128;
+      // P buffer u was last read by the P.V of tile j - 2
+      if (j >= 2 && !(ok = mbar_wait(pv_done(u), ((j >> 1) - 1) & 1, abort_flag, p.err))) break;
+      const uint32_t prow = sbase + C::OFF_P + u * C::P_BYTES + row * 128;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_shared_v4(prow + ((q ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int q = 0; q < 4; ++q)
+        st_shared_v4(prow + (((hf * 4 + q) ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                     pk[4 * q + 3]);
       fence_proxy_async_smem();
       if (rescaled) tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full(u));
     }
-    if (ok && n_kt > 0) ok = mbar_wait(pv_done, (n_kt - 1) & 1, abort_flag, p.err);
+    if (ok && n_kt > 0) ok = mbar_wait(pv_done((n_kt - 1) & 1), ((n_kt - 1) >> 1) & 1, abort_flag, p.err);
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+    // the row sum is the two threads' halves: exchanged through the (now idle) P buffers
+    float* lx = reinterpret_cast<float*>(smem + C::OFF_P);
+    lx[hf * 128 + row] = l;
+    named_bar_sync(1, 256);
+    const float l_row = lx[row] + lx[128 + row];
+    const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
     const int64_t orow = (int64_t)t * p.H + h;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kHead; c0 += 32) {
+    for (int c0 = hf * 128; c0 < hf * 128 + 128; c0 += 32) {
       uint32_t o[32];
       if (n_kt > 0) {
         tmem_ld32(tmem + lane_base + c0, o);
@@ -482,8 +571,8 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
                               pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv, __uint_as_float(o[8 * i + 7]) * inv));
       }
     }
-    if (valid_q && ok && p.lse != nullptr)
-      p.lse[orow] = l > 0.f ? (m_ref + lg2_approx(l)) * 0.69314718055994531f : neg_inf();
+    if (hf == 0 && valid_q && ok && p.lse != nullptr)
+      p.lse[orow] = l_row > 0.f ? (m_ref + lg2_approx(l_row)) * 0.69314718055994531f : neg_inf();
   }
   tc_fence_before();
   __syncthreads();
