@@ -469,11 +469,23 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
-def _per_config(args, dev, stream, flush_l2, peaks):
+def _scaled(spec, scale):
+    """The workload at other sizes (`--scale key=value,...`, for small profiling cases)."""
+    if not scale:
+        return spec
+    kw = {}
+    for item in scale.split(","):
+        key, val = item.split("=")
+        kw[key] = type(getattr(spec, key))(val) if getattr(spec, key) is not None else int(val)
+    return spec.scaled(**kw)
+
+
+def _per_config(args, dev, stream, flush_l2, peaks, names=("tiny", "prefill", "ragged", "indexshare", "csa_flash",
+                                                           "csa_pro")):
     out = {}
     steps = max(3, min(args.steps, 20))
-    for name in ("tiny", "prefill", "ragged", "indexshare", "csa_flash", "csa_pro"):
-        spec = W.SPECS[name]
+    for name in names:
+        spec = _scaled(W.SPECS[name], args.scale)
         run = _Run(spec, dev)
         step_ms = run.time_steps(steps, args.warmup, flush_l2, stream)
         kern_ms = run.kernel_ms(steps, flush_l2, stream)
@@ -607,7 +619,7 @@ def _mha_config(args, dev, stream, flush_l2, peaks):
     import oracle
     from long_context_lightning_gb300 import SparseMHA, _lib
     from long_context_lightning_gb300 import accounting as A
-    spec = W.SPECS["mha"]
+    spec = _scaled(W.SPECS["mha"], args.scale)
     run = _Run(spec, dev)
     wl, sa = run.wl, run.sa
     T, H, k = wl.total_q, spec.heads, spec.topk
@@ -701,6 +713,27 @@ def _mha_config(args, dev, stream, flush_l2, peaks):
     }
 
 
+def run_only(args):
+    """One workload's per-config entry alone (a small, quick command to profile)."""
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    peaks = _peaks_all()
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2(i):
+        flush.fill_(i)
+
+    if args.only == "mha":
+        entry = _mha_config(args, dev, stream, flush_l2, peaks)
+    elif args.only == "hisparse":
+        entry = _hisparse(args, dev, stream, flush_l2)
+    else:
+        entry = _per_config(args, dev, stream, flush_l2, peaks, names=(args.only,))[args.only]
+    print(json.dumps({"only": args.only, "scale": args.scale, "entry": entry}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -708,6 +741,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-per-config", action="store_true", help="time the decode headline only")
+    ap.add_argument("--only", default=None,
+                    help="time one other workload alone (tiny, prefill, ragged, indexshare, csa_flash, csa_pro, mha, "
+                         "hisparse) and print its entry; for profiling")
+    ap.add_argument("--scale", default=None, help="with --only: workload sizes to change, e.g. ctx_len=32768,q_per_seq=1024")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -720,6 +757,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.only:
+            run_only(args)
         else:
             run_gpu(args, rank, world, local_rank)
     finally:
