@@ -180,9 +180,11 @@ def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: fl
 # A source that has changed since makes the figure stale: it is reported as
 # null.  Captured with
 #   ncu --set full --clock-control none -k regex:<kernel>_kernel -s 2 -c 1 \
-#       -o <report> python bench.py --steps 5 --warmup 3
+#       -o <report> python bench.py --steps 5 --warmup 3 --no-per-config
 NCU_TRAFFIC = {
-    ("decode", "indexer"): ("indexer.cu", "f2c2c4f582978c1a", 275527424.0),
+    ("decode", "indexer"): ("indexer.cu", "9168a47dab63d1da", 275455488.0),
+    ("decode", "topk"): ("topk.cu", "dfb51a1062365d6c", 4273664.0),
+    ("decode", "sparse_mla"): ("sparse_mla.cu", "1a5e7a3244462a12", 82912512.0),
 }
 
 
