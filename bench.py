@@ -8,7 +8,10 @@ Metric: query tokens/s, whole job (all ranks).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
 --impl reference times the float64 CPU oracle (the only reference this
-project has) on a bounded sample of the same workload.
+project has) on a bounded sample of the same workload.  `e2e` is a decode step
+as a server runs it: the step's queries and the new tokens' cache rows copied
+from pinned host memory, appended into the resident caches, the forward, and
+the results copied back.
 Under torchrun each rank runs its own 32-sequence batch (weak scaling, no
 collective on the data path); rank 0 prints one JSON line.
 
@@ -394,31 +397,43 @@ def run_gpu(args, rank, world, local_rank):
     kern_ms = run.kernel_ms(min(args.steps, 200), flush_l2, stream)
     clk = clocks.stop()
 
-    # end to end through the public API: inputs from pinned host memory, results back
-    host_in = [t.cpu().pin_memory() for t in
-               (wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.seq_start, *wl.q, *wl.kv)]
-    dev_in = [wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.seq_start, *wl.q, *wl.kv]
+    # end to end through the public API, as a decode step receives its inputs:
+    # the step's queries, head weights and lengths and the new tokens' indexer
+    # keys and latent rows come from pinned host memory, the rows are appended
+    # into the resident caches (dsa_cache_append), the forward runs, and the
+    # indices, outputs and LSE are read back.  The appended rows are the rows
+    # already at the query positions, so every step computes the same result.
+    from long_context_lightning_gb300 import _lib as lib
+    seq, pos = wl.query_positions()
+    at = torch.cat([W.pool_rows(wl, b, torch.tensor([p_])) for b, p_ in zip(seq, pos)]).to(dev)
+    new_k = wl.k_idx[at].clone()
+    new_c = [kv[at].clone() for kv in wl.kv]
+    dev_in = [wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, *wl.q, new_k, *new_c]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
     host_out = [sa.idx.cpu().pin_memory()] + [o.cpu().pin_memory() for o in sa.outs] + \
                [x.cpu().pin_memory() for x in sa.lses]
     dev_out = [sa.idx] + list(sa.outs) + list(sa.lses)
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
     n_e2e = max(3, min(args.steps, 20))
-    for _ in range(2):
+
+    def e2e_step():
         for h, d in zip(host_in, dev_in):
             d.copy_(h, non_blocking=True)
+        lib.cache_append(sa.batch, new_k, sa.indexer.k, sa.workspace)
+        for layer, c in zip(sa.layers, new_c):
+            lib.cache_append(sa.batch, c, layer.kv, sa.workspace)
         sa.forward()
         for h, d in zip(host_out, dev_out):
             h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(n_e2e):
-        for h, d in zip(host_in, dev_in):
-            d.copy_(h, non_blocking=True)
-        sa.forward()
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / n_e2e
@@ -461,7 +476,10 @@ def run_gpu(args, rank, world, local_rank):
                           "frac": all_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm,
                           "algorithmic_bytes_per_step": all_bytes},
         "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "query tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "step": "h2d of the step's queries, head weights, lengths and new tokens' cache rows (pinned host "
+                        "memory) -> dsa_cache_append into the resident caches -> dsa_forward -> d2h of indices, "
+                        "outputs and LSE; no L2 flush (the step streams > 349 MB, more than the 129 MB L2)"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed_region": wall,
