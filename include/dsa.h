@@ -425,7 +425,9 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
  * operand transposed (as the attention value and probability operands are).
  * `swizzle_bytes` is 128 (128-byte swizzled atoms of 64 K-elements) or 64
  * (64-byte swizzled atoms of 32 K-elements, K-major operands only, the way the
- * attention stages its rope halves).
+ * attention stages its rope halves), or 0: A is read from tensor memory (row m
+ * in lane m, two elements per 32-bit column, the way MHA-mode attention feeds
+ * its probabilities), B 128-byte swizzled; a_mn_major must be 0.
  *
  * dsa_selftest_topk_max_cluster: caps the thread-block cluster the top-k
  * launches use on the current device at `max_cluster` blocks (1, 2, 4, 8 or

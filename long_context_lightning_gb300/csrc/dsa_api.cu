@@ -283,7 +283,7 @@ namespace {
 // sw64 the operands are K-major in 64-byte-swizzled atoms, two K-blocks of 32.
 __global__ void __launch_bounds__(128, 1)
     selftest_mma_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* D, int a_mn, int b_mn, int sw64,
-                        int* err) {
+                        int a_tmem, int* err) {
   __shared__ __align__(1024) uint8_t sa[128 * 128];  // 16 KB
   __shared__ __align__(1024) uint8_t sb[64 * 128];   // 8 KB
   __shared__ __align__(8) uint64_t bar;
@@ -325,17 +325,37 @@ __global__ void __launch_bounds__(128, 1)
   }
   fence_proxy_async_smem();
   if (warp == 0) {
-    tmem_alloc(smem_u32(&tslot), 64);
+    tmem_alloc(smem_u32(&tslot), 128);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tslot;
+  if (a_tmem) {
+    // A row m into lane m, columns 64..95: element pairs (2c, 2c+1) of the row in column c
+    const int m = warp * 32 + lane;
+    uint32_t r[32];
+    for (int c = 0; c < 32; ++c) {
+      const uint32_t lo = __bfloat16_as_ushort(A[m * 64 + 2 * c]), hi = __bfloat16_as_ushort(A[m * 64 + 2 * c + 1]);
+      r[c] = lo | (hi << 16);
+    }
+    tmem_st32(tmem + ((uint32_t)(warp * 32) << 16) + 64, r);
+    tmem_wait_st();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (tid == 0) {
     const uint32_t idesc = mma_idesc_bf16(128, 64, a_mn != 0, b_mn != 0);
     for (int ks = 0; ks < 4; ++ks) {
       uint64_t ad, bd;
+      if (a_tmem) {
+        bd = b_mn ? smem_desc_sw128(smem_u32(sb) + ks * 2048, 8192, 1024)
+                  : smem_desc_sw128(smem_u32(sb) + ks * 32, 16, 1024);
+        mma_bf16_ts(tmem, tmem + 64 + ks * 8, bd, idesc, ks != 0);
+        continue;
+      }
       if (sw64) {
         ad = smem_desc_sw64(smem_u32(sa) + (ks / 2) * 8192 + (ks % 2) * 32, 512);
         bd = smem_desc_sw64(smem_u32(sb) + (ks / 2) * 4096 + (ks % 2) * 32, 512);
@@ -363,7 +383,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -613,13 +633,14 @@ dsa_status_t dsa_sparse_mla_fwd_noalloc(const dsa_batch_t* batch, const dsa_mla_
 dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_mn_major, int32_t b_mn_major,
                               int32_t swizzle_bytes, cudaStream_t stream) {
   if (a == nullptr || b == nullptr || d == nullptr) return DSA_ERR_INVALID_ARG;
-  if (swizzle_bytes != 128 && swizzle_bytes != 64) return DSA_ERR_INVALID_ARG;
+  if (swizzle_bytes != 128 && swizzle_bytes != 64 && swizzle_bytes != 0) return DSA_ERR_INVALID_ARG;
   if (swizzle_bytes == 64 && (a_mn_major || b_mn_major)) return DSA_ERR_UNSUPPORTED;
+  if (swizzle_bytes == 0 && a_mn_major) return DSA_ERR_UNSUPPORTED;
   DeviceInfo dev;
   if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
   selftest_mma_kernel<<<1, 128, 0, stream>>>(static_cast<const __nv_bfloat16*>(a),
                                               static_cast<const __nv_bfloat16*>(b), d, a_mn_major, b_mn_major,
-                                              swizzle_bytes == 64, dev.err);
+                                              swizzle_bytes == 64, swizzle_bytes == 0, dev.err);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -25,8 +25,8 @@
 //            of two TMEM buffers, online softmax in fp32 over the selected
 //            keys only (a per-row reference that moves when a score passes it
 //            by more than 2^8, so O is rescaled in TMEM only then), P in bf16
-//            to one of two shared buffers, O += P V (M = 128, N = 256, K = 64)
-//            in TMEM.  Warp 0 streams Q once and K/V tiles through two stages
+//            into one of two tensor-memory buffers (each thread its own lane),
+//            O += P V (M = 128, N = 256, K = 64) with P read from tensor memory.  Warp 0 streams Q once and K/V tiles through two stages
 //            with TMA, warp 1 issues the MMAs, warps 2-9 do the softmax: two
 //            threads per query row, both finding the row maximum over the
 //            tile's 64 keys, each exponentiating 32 of them and owning 128 of
@@ -219,17 +219,18 @@ struct AttCfg {
   static constexpr int Q_BYTES = 128 * kHead * 2;        // 64 KB: 4 blocks [128 x 64]
   static constexpr int K_BYTES = 64 * kHead * 2;         // 32 KB: 4 blocks [64 x 64]
   static constexpr int V_BYTES = 64 * kHead * 2;         // 32 KB: 4 value blocks [64 keys x 64]
-  static constexpr int STAGE_BYTES = K_BYTES + V_BYTES;
-  static constexpr int P_BYTES = 128 * 64 * 2;           // 16 KB: [128 queries x 64 keys], two buffers
+  static constexpr int K_STAGES = 3;
+  static constexpr int V_STAGES = 2;
   static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = OFF_Q + Q_BYTES;
-  static constexpr int OFF_P = OFF_KV + 2 * STAGE_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int N_BARS = 18;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + K_STAGES * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + V_STAGES * V_BYTES;
+  static constexpr int N_BARS = 20;
   static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
   static constexpr int SMEM_BYTES = OFF_MISC + 32 + 1024;
-  static constexpr int TMEM_COLS = 512;                  // O: 256 columns, S: two buffers of 64
-  static constexpr uint32_t S_COL = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr uint32_t S_COL = 256;                 // O: columns 0..255; S: two buffers of 64
+  static constexpr uint32_t P_COL = 384;                 // P: two buffers of 32 (64 keys, bf16 pairs)
 };
 
 struct AttParams {
@@ -257,15 +258,15 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const uint32_t q_full = smem_u32(bars + 0);
-  auto k_full = [&](int s) { return smem_u32(bars + 1 + s); };
-  auto k_empty = [&](int s) { return smem_u32(bars + 3 + s); };
-  auto v_full = [&](int s) { return smem_u32(bars + 5 + s); };
-  auto v_empty = [&](int s) { return smem_u32(bars + 7 + s); };
-  auto s_full = [&](int u) { return smem_u32(bars + 9 + u); };
-  auto s_free = [&](int u) { return smem_u32(bars + 11 + u); };
-  auto p_full = [&](int u) { return smem_u32(bars + 13 + u); };
-  auto pv_done = [&](int u) { return smem_u32(bars + 15 + u); };
-  const uint32_t drain = smem_u32(bars + 17);
+  auto k_full = [&](int s) { return smem_u32(bars + 1 + s); };    // 3
+  auto k_empty = [&](int s) { return smem_u32(bars + 4 + s); };   // 3
+  auto v_full = [&](int s) { return smem_u32(bars + 7 + s); };    // 2
+  auto v_empty = [&](int s) { return smem_u32(bars + 9 + s); };   // 2
+  auto s_full = [&](int u) { return smem_u32(bars + 11 + u); };
+  auto s_free = [&](int u) { return smem_u32(bars + 13 + u); };
+  auto p_full = [&](int u) { return smem_u32(bars + 15 + u); };
+  auto pv_done = [&](int u) { return smem_u32(bars + 17 + u); };
+  const uint32_t drain = smem_u32(bars + 19);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_wait();  // the plan and the masks are complete from here on
@@ -278,9 +279,11 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < C::K_STAGES; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(v_full(s), 1);
       mbar_init(v_empty(s), 1);
       mbar_init(s_full(s), 1);
@@ -297,10 +300,8 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
   }
   // value stages start as zeros: a key that no query selects contributes P = 0
   // times whatever its stage holds, which must not be a NaN pattern
-  for (int i = threadIdx.x; i < 2 * C::V_BYTES / 16; i += C::THREADS) {
-    const int s = i / (C::V_BYTES / 16), o = i % (C::V_BYTES / 16);
-    st_shared_v4(sbase + C::OFF_KV + s * C::STAGE_BYTES + C::K_BYTES + o * 16, 0, 0, 0, 0);
-  }
+  for (int i = threadIdx.x; i < C::V_STAGES * C::V_BYTES / 16; i += C::THREADS)
+    st_shared_v4(sbase + C::OFF_V + i * 16, 0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -317,15 +318,16 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       mbar_arrive_expect_tx(q_full, C::Q_BYTES);
       for (int kb = 0; kb < 4; ++kb) tma_load_3d(sbase + C::OFF_Q + kb * 16384, &tm_q, q_full, kb * 64, h, q0);
       // keys and values have stages of their own: a key stage is free once
-      // its S = Q K^T is done, a value stage only after its P.V, so keys are
-      // loaded one tile ahead of values.  A 64-key tile is one 64-token page.
+      // its S = Q K^T is done, a value stage only after its P.V, so keys (three
+      // stages) are loaded two tiles ahead of values (two stages).  A 64-key
+      // tile is one 64-token page.
       const int32_t* pt = p.kv.paged ? p.kv.page_table + (int64_t)b * p.kv.pt_stride : nullptr;
       const int64_t start = p.kv.paged ? 0 : __ldg(p.kv.seq_start + b);
-      int64_t row_of[2] = {0, 0};
-      bool valid_of[2] = {false, false};
+      int64_t row_of[3] = {0, 0, 0};
+      bool valid_of[3] = {false, false, false};
       int issued_k = 0, issued_v = 0;
       auto issue_k = [&](int j) -> bool {
-        const int s = j & 1;
+        const int s = j % 3;
         int64_t row0;
         bool valid;
         if (p.kv.paged) {
@@ -338,8 +340,8 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
         }
         row_of[s] = row0;
         valid_of[s] = valid;
-        if (j >= 2 && !mbar_wait(k_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
-        const uint32_t dst = sbase + C::OFF_KV + s * C::STAGE_BYTES;
+        if (j >= 3 && !mbar_wait(k_empty(s), ((j / 3) - 1) & 1, abort_flag, p.err)) return false;
+        const uint32_t dst = sbase + C::OFF_K + s * C::K_BYTES;
         if (valid) {
           mbar_arrive_expect_tx(k_full(s), C::K_BYTES);
           for (int kb = 0; kb < 4; ++kb) tma_load_3d(dst + kb * 8192, &tm_k, k_full(s), kb * 64, h, (int32_t)row0);
@@ -351,28 +353,28 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
         return true;
       };
       auto issue_v = [&](int j) -> bool {
-        const int s = j & 1;
+        const int s = j & 1, r = j % 3;
         if (j >= 2 && !mbar_wait(v_empty(s), ((j >> 1) - 1) & 1, abort_flag, p.err)) return false;
-        const uint32_t dst = sbase + C::OFF_KV + s * C::STAGE_BYTES + C::K_BYTES;
-        if (valid_of[s]) {
+        const uint32_t dst = sbase + C::OFF_V + s * C::V_BYTES;
+        if (valid_of[r]) {
           mbar_arrive_expect_tx(v_full(s), C::V_BYTES);
           for (int kb = 0; kb < 4; ++kb)
-            tma_load_3d(dst + kb * 8192, &tm_v, v_full(s), kb * 64, h, (int32_t)row_of[s]);
+            tma_load_3d(dst + kb * 8192, &tm_v, v_full(s), kb * 64, h, (int32_t)row_of[r]);
         } else {
           mbar_arrive(v_full(s));
         }
         ++issued_v;
         return true;
       };
-      if (issue_k(0)) {
+      if (issue_k(0) && (n_kt < 2 || issue_k(1))) {
         for (int j = 0; j < n_kt; ++j) {
-          if (j + 1 < n_kt && !issue_k(j + 1)) break;
+          if (j + 2 < n_kt && !issue_k(j + 2)) break;
           if (!issue_v(j)) break;
         }
       }
       if (*abort_flag) {
         mbar_wait_drain(q_full, 0);
-        for (int j = std::max(0, issued_k - 2); j < issued_k; ++j) mbar_wait_drain(k_full(j & 1), (j >> 1) & 1);
+        for (int j = std::max(0, issued_k - 3); j < issued_k; ++j) mbar_wait_drain(k_full(j % 3), (j / 3) & 1);
         for (int j = std::max(0, issued_v - 2); j < issued_v; ++j) mbar_wait_drain(v_full(j & 1), (j >> 1) & 1);
       }
     }
@@ -383,31 +385,30 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       const uint32_t idesc_o = mma_idesc_bf16(128, kHead, false, true);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.err);
       auto issue_s = [&](int j) {
-        const int u = j & 1;
-        const uint32_t kbase = sbase + C::OFF_KV + u * C::STAGE_BYTES;
+        const int u = j & 1, ks3 = j % 3;
+        const uint32_t kbase = sbase + C::OFF_K + ks3 * C::K_BYTES;
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16(tmem + C::S_COL + u * 64, smem_desc_sw128(sbase + C::OFF_Q + kb * 16384 + ks * 32, 16, 1024),
                      smem_desc_sw128(kbase + kb * 8192 + ks * 32, 16, 1024), idesc_s, (kb | ks) != 0);
-        mma_commit(k_empty(u));
+        mma_commit(k_empty(ks3));
         mma_commit(s_full(u));
       };
       auto issue_pv = [&](int j) {
         const int u = j & 1;
-        const uint32_t vbase = sbase + C::OFF_KV + u * C::STAGE_BYTES + C::K_BYTES;
-        const uint32_t pbase = sbase + C::OFF_P + u * C::P_BYTES;
+        const uint32_t vbase = sbase + C::OFF_V + u * C::V_BYTES;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          mma_bf16(tmem, smem_desc_sw128(pbase + ks * 32, 16, 1024),
-                   smem_desc_sw128(vbase + ks * 2048, 8192, 1024), idesc_o, (j | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks)  // P from tensor memory: 16 keys = 8 columns per step
+          mma_bf16_ts(tmem, tmem + C::P_COL + u * 32 + ks * 8, smem_desc_sw128(vbase + ks * 2048, 8192, 1024),
+                      idesc_o, (j | ks) != 0);
         mma_commit(v_empty(u));
         mma_commit(pv_done(u));
       };
       auto ready_s = [&](int j) {
         const int u = j & 1;
-        return mbar_test_wait(k_full(u), (j >> 1) & 1) &&
+        return mbar_test_wait(k_full(j % 3), (j / 3) & 1) &&
                (j < 2 || mbar_test_wait(s_free(u), ((j >> 1) - 1) & 1));
       };
       auto ready_pv = [&](int j) {
@@ -530,22 +531,18 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
         pk[c >> 1] = w;
       }
       l += lsum;
-      // P buffer u was last read by the P.V of tile j - 2
+      // P buffer u (tensor memory) was last read by the P.V of tile j - 2
       if (j >= 2 && !(ok = mbar_wait(pv_done(u), ((j >> 1) - 1) & 1, abort_flag, p.err))) break;
-      const uint32_t prow = sbase + C::OFF_P + u * C::P_BYTES + row * 128;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        st_shared_v4(prow + (((hf * 4 + q) ^ (row & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                     pk[4 * q + 3]);
-      fence_proxy_async_smem();
-      if (rescaled) tmem_wait_st();
+      tc_fence_after();
+      tmem_st16(tmem + lane_base + C::P_COL + u * 32 + hf * 16, pk);  // this thread's 32 keys of the row
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full(u));
     }
     if (ok && n_kt > 0) ok = mbar_wait(pv_done((n_kt - 1) & 1), ((n_kt - 1) >> 1) & 1, abort_flag, p.err);
     tc_fence_after();
-    // the row sum is the two threads' halves: exchanged through the (now idle) P buffers
-    float* lx = reinterpret_cast<float*>(smem + C::OFF_P);
+    // the row sum is the two threads' halves: exchanged through the (now idle) value stages
+    float* lx = reinterpret_cast<float*>(smem + C::OFF_V);
     lx[hf * 128 + row] = l;
     named_bar_sync(1, 256);
     const float l_row = lx[row] + lx[128 + row];

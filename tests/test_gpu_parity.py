@@ -23,7 +23,8 @@ def lib():
 # ------------------------------------------------ device machinery checks ---
 
 @pytest.mark.parametrize("a_mn,b_mn,sw", [(False, False, 128), (True, True, 128), (True, False, 128),
-                                          (False, True, 128), (False, False, 64)])
+                                          (False, True, 128), (False, False, 64),
+                                          (False, False, 0), (False, True, 0)])  # 0: A from tensor memory
 def test_selftest_mma_tile(lib, a_mn, b_mn, sw):
     g = torch.Generator().manual_seed(7)
     a = torch.randint(-4, 5, (128, 64), generator=g).to(torch.bfloat16).cuda()
