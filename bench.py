@@ -616,6 +616,7 @@ def _hisparse(args, dev, stream, flush_l2):
     cold_us = statistics.median(cold)
     del run, hc, host
     torch.cuda.empty_cache()
+    seq_us, ovl_us = _hisparse_two_layers(dev, stream, flush_l2)
     return {
         "workload": f"decode B={spec.batch} x ctx {spec.ctx_len}: layer-0 latent pool ({spec.batch * spec.ctx_len}"
                     f" rows x {row_bytes} B) in pinned host memory, HBM slot pool of {capacity} rows",
@@ -626,6 +627,10 @@ def _hisparse(args, dev, stream, flush_l2):
         "sparse_mla_over_slots_us": statistics.median(mla_slots),
         "sparse_mla_over_pool_us": statistics.median(mla_pool),
         "launches_per_fetch": 7,
+        "two_layers_sequential_us": seq_us,
+        "two_layers_overlapped_us": ovl_us,
+        "two_layers": "decode-like step of two layers sharing one selection: fetch L0, sparse MLA L0, fetch L1, "
+                      "sparse MLA L1 on one stream, against L1's fetch on a second stream beside L0's sparse MLA",
         "cpu_baseline": {"value": sum(len(r) for r in reqs) / dt, "unit": "requested rows/s", "kind": "oracle",
                          "cores": 1, "sample": f"LRU bookkeeping of the {len(reqs)}-step trace, python, {dt:.2f} s"},
     }
@@ -752,6 +757,76 @@ def run_only(args):
     else:
         entry = _per_config(args, dev, stream, flush_l2, peaks, names=(args.only,))[args.only]
     print(json.dumps({"only": args.only, "scale": args.scale, "entry": entry}), flush=True)
+
+
+def _hisparse_two_layers(dev, stream, flush_l2):
+    """Two layers of the decode workload, each with its latent pool in pinned
+    host memory and an HBM row cache, one selection for both (IndexShare): a
+    decode-like step (every eighth entry of the selection replaced) timed with
+    the layers in sequence on one stream, and with layer 1's fetch on a second
+    stream beside layer 0's sparse MLA (the loads for one layer overlap the
+    previous layer's attention)."""
+    from long_context_lightning_gb300 import HiSparseCache, _lib
+    spec = W.SPECS["decode"].scaled(n_layers=2)
+    run = _Run(spec, dev)
+    wl, sa = run.wl, run.sa
+    T, k = wl.total_q, spec.topk
+    hcs = [HiSparseCache(wl.kv[layer].cpu().pin_memory(), 262144, seq_start=wl.seq_start) for layer in range(2)]
+    slots = [torch.empty((T, k), dtype=torch.int32, device=dev) for _ in range(2)]
+    layers = [hc.layer(wl.q[layer], spec.d_v, spec.scale) for layer, hc in enumerate(hcs)]
+    outs = [torch.empty_like(o) for o in sa.outs]
+    g = torch.Generator(device=dev)
+    g.manual_seed(spec.seed * 1000 + 78)
+    n = wl.seq_lens.to(torch.int64).view(T, 1)
+    sel = sa.idx.clone()
+    side = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)   # noqa: E731
+
+    def next_sel():
+        fresh = (torch.rand((T, k), generator=g, device=dev) * n).to(torch.int32)
+        sel[:, ::8] = fresh[:, ::8]
+
+    def mla(layer):
+        _lib.sparse_mla_fwd(sa.batch, layers[layer], slots[layer], k, outs[layer], None, sa.workspace)
+
+    def sequential():
+        for layer in range(2):
+            hcs[layer].fetch(sa.batch, sel, k, slots[layer])
+            mla(layer)
+
+    def overlapped():
+        hcs[0].fetch(sa.batch, sel, k, slots[0])
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        side.wait_event(ready)
+        with torch.cuda.stream(side):
+            hcs[1].fetch(sa.batch, sel, k, slots[1], stream=side)
+        mla(0)
+        done = torch.cuda.Event()
+        done.record(side)
+        stream.wait_event(done)
+        mla(1)
+
+    for fn in (sequential, overlapped):   # fill both caches, warm the code
+        fn()
+    torch.cuda.synchronize(dev)
+    res = {}
+    for name, fn in (("sequential", sequential), ("overlapped", overlapped)):
+        ts = []
+        for i in range(8):
+            next_sel()
+            flush_l2(i)
+            a, b = ev(), ev()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        res[name] = statistics.median(ts)
+    run.check("hisparse two layers")
+    del run, hcs
+    torch.cuda.empty_cache()
+    return res["sequential"], res["overlapped"]
 
 
 def main():
