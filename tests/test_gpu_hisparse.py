@@ -192,3 +192,37 @@ def test_unpinned_host_pool_is_rejected(lib):
     with pytest.raises(lib.DsaError) as e:
         lib.hisparse_fetch(hs, sa.batch, host_cache, sa.idx, spec.topk, slots, sa.workspace)
     assert e.value.status == lib.DSA_ERR_INVALID_ARG
+
+
+def test_full_size_decode_trace(lib):
+    # the decode workload (32 x 32768, top-2048): layer 0's 1,048,576 rows in pinned
+    # host memory, 262,144 HBM slots; the indexer's selection, then decode-like
+    # steps that replace every eighth entry
+    spec = W.SPECS["decode"]
+    capacity = 262144
+    wl, sa, host, hc = _setup(lib, spec, capacity)
+    wl_cpu = wl.to("cpu", kv_too=False)
+    k, T = spec.topk, wl.total_q
+    idx0, _, _ = sa.forward()
+    sel = idx0.clone()
+    g = torch.Generator(device="cuda").manual_seed(5)
+    n = wl.seq_lens.to(torch.int64).view(T, 1)
+    slots = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    lru = oracle.HiSparseLRU(capacity)
+    out_a = torch.empty_like(sa.outs[0])
+    out_b = torch.empty_like(sa.outs[0])
+    for step in range(1, 5):
+        if step > 1:
+            fresh = (torch.rand((T, k), generator=g, device="cuda") * n).to(torch.int32)
+            sel[:, ::8] = fresh[:, ::8]
+        hc.fetch(sa.batch, sel, k, slots)
+        assert lib.check_device_error() == lib.DSA_OK
+        hits, misses, evicted = lru.step(_oracle_rows(wl_cpu, sel.cpu()))
+        assert hc.stats() == dict(steps=step, requested=len(hits) + len(misses), hits=len(hits),
+                                  misses=len(misses), evicted=len(evicted), overflow=0), f"step {step}"
+        assert hc.resident() == list(lru.order), f"step {step}: LRU order"
+        lib.sparse_mla_fwd(sa.batch, sa.layers[0], sel, k, out_a, None, sa.workspace)
+        lib.sparse_mla_fwd(sa.batch, hc.layer(wl.q[0], spec.d_v, spec.scale), slots, k, out_b, None, sa.workspace)
+        torch.cuda.synchronize()
+        assert lib.check_device_error() == lib.DSA_OK
+        assert torch.equal(out_a, out_b), f"step {step}"
