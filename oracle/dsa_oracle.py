@@ -337,7 +337,7 @@ def requested_rows(wl, idx_rows) -> list:
 
 def attention_on_set(wl, t: int, layer: int, sel: np.ndarray, kv_rows_fetch=None):
     """Sparse MLA of query t over an externally supplied index set `sel`
-    (used to judge the GPU outputs on the GPU's own selection)."""
+    (used to check the GPU outputs on the GPU's own selection)."""
     seq, pos = _query_table(wl)
     b = seq[t]
     sel = np.asarray(sel, dtype=np.int64)

@@ -1,4 +1,4 @@
-"""Shared test helpers: run the CUDA path on a workload and judge it against the oracle."""
+"""Shared test helpers: run the CUDA path on a workload and compare it with the oracle."""
 from __future__ import annotations
 
 import numpy as np
@@ -50,7 +50,7 @@ class SeqKeys:
         return oracle.indexer_scores(oracle.bf16_to_f64(wl.q_idx[t]), oracle.f32_to_f64(wl.w[t]), self.keys[:n])
 
 
-def judge_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=None, seq_keys=None):
+def compare_forward(wl, idx, outs, lses, queries, exact_idx=False, kv_rows_fetch=None, seq_keys=None):
     """Compare the GPU result of `queries` with the oracle.
 
     Indices: bit-exact when `exact_idx` (integer indexer inputs), else the band

@@ -9,7 +9,7 @@ import torch
 
 import dsa_workloads as W
 import oracle
-from helpers import judge_forward, make_sa
+from helpers import compare_forward, make_sa
 
 pytestmark = pytest.mark.gpu
 
@@ -29,7 +29,7 @@ def test_compressed_full_size(lib, name):
     idx, outs, lses = make_sa(wl).forward()
     torch.cuda.synchronize()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 @pytest.mark.parametrize("name", ["csa_flash", "csa_pro"])
@@ -41,7 +41,7 @@ def test_compressed_integer_exact(lib, name):
     torch.cuda.synchronize()
     assert lib.check_device_error() == lib.DSA_OK
     cpu = wl.to("cpu")
-    judge_forward(cpu, idx, outs, lses, range(wl.total_q), exact_idx=True)
+    compare_forward(cpu, idx, outs, lses, range(wl.total_q), exact_idx=True)
     # the fused call's fp32 scores are the oracle's, bit for bit, over every visible entry
     scores = sa.scores_view().double().cpu().numpy()
     seq, pos = cpu.query_positions()
@@ -58,7 +58,7 @@ def test_compressed_around_the_dense_threshold_and_partial_blocks(lib, ratio, ct
     wl = W.make_workload(spec, device="cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 def test_compressed_paged_equals_contiguous_bitwise(lib):
@@ -75,4 +75,4 @@ def test_compressed_paged_equals_contiguous_bitwise(lib):
     b_idx, b_out, _ = make_sa(contig).forward()
     assert lib.check_device_error() == lib.DSA_OK
     assert torch.equal(a_idx, b_idx) and torch.equal(a_out[0], b_out[0])
-    judge_forward(wl.to("cpu"), a_idx, a_out, None, range(wl.total_q))
+    compare_forward(wl.to("cpu"), a_idx, a_out, None, range(wl.total_q))

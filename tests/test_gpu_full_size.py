@@ -1,7 +1,7 @@
 """Parity at the five workloads' full sizes, in the launch configuration the
 benchmark times (the same fused call, also replayed from a CUDA graph).
 
-Decode, ragged and IndexShare are judged on every query; the prefill chunk on
+Decode, ragged and IndexShare are checked on every query; the prefill chunk on
 its first and last query plus 254 seeded ones (the oracle scores up to 131072
 keys per query in float64).
 Properties that hold at any size (ascending distinct positions inside the
@@ -13,7 +13,7 @@ import torch
 
 import dsa_workloads as W
 import oracle
-from helpers import SeqKeys, judge_forward, make_sa
+from helpers import SeqKeys, compare_forward, make_sa
 
 pytestmark = pytest.mark.gpu
 
@@ -42,7 +42,7 @@ def test_tiny_full(lib):
     wl = W.make_workload(W.SPECS["tiny"]).to("cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q), exact_idx=True)
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q), exact_idx=True)
 
 
 def test_decode_full_graph_replay(lib):
@@ -64,7 +64,7 @@ def test_decode_full_graph_replay(lib):
     assert torch.equal(sa.idx, first[0]) and torch.equal(sa.outs[0], first[1]) and torch.equal(sa.lses[0], first[2])
     _rows_valid(wl, sa.idx)
     assert torch.isfinite(sa.outs[0].float()).all()
-    judge_forward(wl.to("cpu"), sa.idx, sa.outs, sa.lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), sa.idx, sa.outs, sa.lses, range(wl.total_q))
 
 
 def test_prefill_full_sampled(lib):
@@ -79,7 +79,7 @@ def test_prefill_full_sampled(lib):
     sample = [0, 4095, *(1 + rng.choice(4094, 254, replace=False)).tolist()]
     assert len(set(sample)) == 256
     cpu = wl.to("cpu")
-    judge_forward(cpu, idx, outs, lses, sorted(sample), seq_keys=SeqKeys(cpu, 0, 131072))
+    compare_forward(cpu, idx, outs, lses, sorted(sample), seq_keys=SeqKeys(cpu, 0, 131072))
 
 
 def test_ragged_paged_full(lib):
@@ -90,7 +90,7 @@ def test_ragged_paged_full(lib):
     assert lib.check_device_error() == lib.DSA_OK
     assert (wl.seq_lens <= spec.topk).any() and (wl.seq_lens > spec.topk).any()   # both paths exercised
     _rows_valid(wl, idx)
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 def test_indexshare_full(lib):
@@ -101,4 +101,4 @@ def test_indexshare_full(lib):
     assert lib.check_device_error() == lib.DSA_OK
     _rows_valid(wl, idx)
     # keep the four 2.4 GB latent pools on the device; the oracle fetches the rows it needs
-    judge_forward(wl.to("cpu", kv_too=False), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu", kv_too=False), idx, outs, lses, range(wl.total_q))

@@ -20,7 +20,7 @@ import torch
 
 import dsa_workloads as W
 import oracle
-from helpers import SeqKeys, judge_forward, make_sa
+from helpers import SeqKeys, compare_forward, make_sa
 
 pytestmark = pytest.mark.gpu
 
@@ -79,7 +79,7 @@ def test_decode_full_integer_exact(lib):
     tied = _exact_rows(wl, idx, range(T), scores=scores)
     assert tied > 0, "no row tied at its k-th score: the tie rule went untested"
     # attention on that exact set, every query
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(T), exact_idx=True)
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(T), exact_idx=True)
 
 
 def test_prefill_chunk_full_integer_exact(lib):

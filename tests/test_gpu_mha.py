@@ -1,6 +1,6 @@
 """MHA mode on the GPU against the float64 oracle: the per-head up-projection
 of the latent rows (rope dims bit for bit), and attention of every head over
-the GPU's own top-k selection, judged by the output rule; paged and ragged
+the GPU's own top-k selection, checked by the output rule; paged and ragged
 batches, dense rows (context <= k) and sparse rows, empty selections and bad
 indices."""
 import numpy as np

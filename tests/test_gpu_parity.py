@@ -7,7 +7,7 @@ import torch
 
 import dsa_workloads as W
 import oracle
-from helpers import check_output, judge_forward, make_sa, sel_of
+from helpers import check_output, compare_forward, make_sa, sel_of
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +51,7 @@ def test_tiny_forward_exact(lib):
     sa = make_sa(wl)
     idx, outs, lses = sa.forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q), exact_idx=True)
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q), exact_idx=True)
 
 
 def test_tiny_indexer_scores_exact(lib):
@@ -153,7 +153,7 @@ def test_decode_small_contexts(lib, ctx):
     wl = W.make_workload(spec, device="cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 def test_prefill_small_chunk(lib):
@@ -161,7 +161,7 @@ def test_prefill_small_chunk(lib):
     wl = W.make_workload(spec, device="cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, [0, 1, 2, 33, 68, 69])
+    compare_forward(wl.to("cpu"), idx, outs, lses, [0, 1, 2, 33, 68, 69])
 
 
 def test_ragged_paged_small(lib):
@@ -169,7 +169,7 @@ def test_ragged_paged_small(lib):
     wl = W.make_workload(spec, device="cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 def test_indexshare_small(lib):
@@ -177,7 +177,7 @@ def test_indexshare_small(lib):
     wl = W.make_workload(spec, device="cuda")
     idx, outs, lses = make_sa(wl).forward()
     assert lib.check_device_error() == lib.DSA_OK
-    judge_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
+    compare_forward(wl.to("cpu"), idx, outs, lses, range(wl.total_q))
 
 
 # ------------------------------------------------------------- invariants ---

@@ -15,7 +15,7 @@ magnitudes:
 With scale 1/16 a head that sees the staircase has logits step * tile + spread
 (natural log units); a step of 12 is 17.3 in log2 units, past the 2^16 rule.
 
-Every head is judged on its own against the float64 oracle over the same
+Every head is checked on its own against the float64 oracle over the same
 index set (max |err| <= 1e-2 * max |ref| and mean |err| <= 1e-3 * max |ref|,
 per head, stricter than per query), and LSE to 1e-4.
 """
