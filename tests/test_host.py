@@ -40,8 +40,9 @@ def test_library_exports_every_declared_symbol(built):
 
 def test_status_strings_without_gpu(built):
     lib = built.load()
-    for s in range(7):
+    for s in range(8):
         assert lib.dsa_status_string(s).decode().startswith("DSA_")
+    assert "CAPACITY" in lib.dsa_status_string(built.DSA_ERR_CAPACITY).decode()
 
 
 def test_struct_layout_matches_header(built):
@@ -51,6 +52,10 @@ def test_struct_layout_matches_header(built):
     assert ctypes.sizeof(built.Batch) == 32
     assert built.Indexer.k.offset == 16 and ctypes.sizeof(built.Indexer) == 80
     assert built.MlaLayer.kv.offset == 8 and built.MlaLayer.scale.offset == 76
+    assert ctypes.sizeof(built.HiSparse) == 40
+    assert built.HiSparse.slot_pool.offset == 8 and built.HiSparse.state.offset == 32
+    assert ctypes.sizeof(built.MhaLayer) == 136
+    assert built.MhaLayer.v.offset == 64 and built.MhaLayer.n_heads.offset == 120 and built.MhaLayer.scale.offset == 132
 
 
 def test_host_validation_without_gpu(built):
@@ -101,3 +106,69 @@ def test_bench_reference_line_keys():
               "cpu_baseline", "e2e", "config", "dtype"):
         assert k in line
     assert line["impl"] == "reference" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_host_validation_of_the_later_entry_points(built):
+    # every rejection below happens in host code, before any CUDA call
+    lib = built.load()
+    b = built.Batch(2, 2, 1000, 1, 16, 32)          # fake aligned pointers; nothing is dereferenced
+    cache = built.Cache(built.CACHE_CONTIGUOUS, 0, 256, 576, 4000, 64, None, 0)
+    # compressed entries: the ratio must be 1 .. max_seqlen_k
+    ix = built.Indexer(16, 16, built.Cache(built.CACHE_CONTIGUOUS, 0, 256, 128, 4000, 64, None, 0), 64, 128)
+    layer = built.MlaLayer(16, cache, 64, 576, 512, 0.0625)
+    arr = (built.MlaLayer * 1)(layer)
+    outs = (ctypes.c_void_p * 1)(16)
+    for ratio in (0, 1001):
+        st = lib.dsa_forward_compressed(ctypes.byref(b), ratio, ctypes.byref(ix), 2048, 1, arr, 16, 2048, outs,
+                                        None, 16, 1 << 30, None, None)
+        assert st == built.DSA_ERR_INVALID_ARG
+    # cache append: no cache, odd row width
+    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 576, None, 16, 1 << 20, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 570, ctypes.byref(cache), 16, 1 << 20,
+                                None) == built.DSA_ERR_INVALID_ARG
+    # HiSparse sizing and argument checks
+    assert lib.dsa_hisparse_state_bytes(0, 100) == 0 and lib.dsa_hisparse_state_bytes(16, 0) == 0
+    assert lib.dsa_hisparse_state_bytes(16, 100) >= 12 * 100 + 24 * 16
+    assert lib.dsa_hisparse_workspace_size(None, 2048, 16) == 0
+    assert lib.dsa_hisparse_workspace_size(ctypes.byref(b), 2048, 0) == 0
+    small = lib.dsa_hisparse_workspace_size(ctypes.byref(b), 2048, 16)
+    assert 0 < small < lib.dsa_hisparse_workspace_size(ctypes.byref(b), 2048, 1 << 20)   # chunk counts grow
+    assert lib.dsa_hisparse_reset(None, None) == built.DSA_ERR_INVALID_ARG
+    hs = built.HiSparse(16, 570, 256, 576, 4000, 512)              # row width not a multiple of 8
+    assert lib.dsa_hisparse_reset(ctypes.byref(hs), None) == built.DSA_ERR_INVALID_ARG
+    hs = built.HiSparse(16, 576, 256, 576, 4000, 512)
+    slots = 16
+    st = lib.dsa_hisparse_fetch(None, ctypes.byref(b), ctypes.byref(cache), 16, 2048, 2048, slots, 2048, 16,
+                                1 << 20, None)
+    assert st == built.DSA_ERR_INVALID_ARG
+    rows_cache = built.Cache(built.CACHE_ROWS, 0, 256, 576, 4000, None, None, 0)   # a slot pool is not a host pool
+    st = lib.dsa_hisparse_fetch(ctypes.byref(hs), ctypes.byref(b), ctypes.byref(rows_cache), 16, 2048, 2048, slots,
+                                2048, 16, 1 << 20, None)
+    assert st == built.DSA_ERR_INVALID_ARG
+    st = lib.dsa_hisparse_fetch(ctypes.byref(hs), ctypes.byref(b), ctypes.byref(cache), 16, 2048, 2048, slots,
+                                2048, 16, 64, None)                # workspace too small
+    assert st == built.DSA_ERR_WORKSPACE
+    # MHA mode: projection arguments, fixed head sizes, context limit, key/value addressing
+    assert lib.dsa_mha_project(None, 576, 10, 64, 16, 16, 16, 16, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_mha_project(16, 500, 10, 64, 16, 16, 16, 16, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_mha_project(16, 576, 10, 0, 16, 16, 16, 16, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_mha_project(16, 576, 0, 64, 16, 16, 16, 16, None) == built.DSA_OK   # nothing to do
+    big = built.Batch(2, 2, 200000, 1, 16, 32)
+    assert lib.dsa_mha_workspace_size(ctypes.byref(big)) == 0
+    assert lib.dsa_mha_workspace_size(ctypes.byref(b)) > 0
+    kc = built.Cache(built.CACHE_CONTIGUOUS, 0, 256, 64 * 256, 4000, 64, None, 0)
+    vc = built.Cache(built.CACHE_CONTIGUOUS, 0, 512, 64 * 256, 4000, 64, None, 0)
+    ws = lib.dsa_mha_workspace_size(ctypes.byref(b))
+
+    def mha(layer_):
+        return lib.dsa_sparse_mha_fwd(ctypes.byref(b), ctypes.byref(layer_), 16, 2048, 2048, 16, None, 16, ws, None)
+
+    assert mha(built.MhaLayer(16, kc, vc, 64, 128, 256, 0.0625)) == built.DSA_ERR_UNSUPPORTED   # head dim
+    assert mha(built.MhaLayer(16, kc, vc, 200, 256, 256, 0.0625)) == built.DSA_ERR_UNSUPPORTED  # heads
+    other = built.Cache(built.CACHE_CONTIGUOUS, 0, 512, 64 * 256, 4000, 128, None, 0)         # other addressing
+    assert mha(built.MhaLayer(16, kc, other, 64, 256, 256, 0.0625)) == built.DSA_ERR_INVALID_ARG
+    rows = built.Cache(built.CACHE_ROWS, 0, 256, 64 * 256, 4000, None, None, 0)
+    assert mha(built.MhaLayer(16, rows, rows, 64, 256, 256, 0.0625)) == built.DSA_ERR_INVALID_ARG
+    st = lib.dsa_sparse_mha_fwd(ctypes.byref(b), ctypes.byref(built.MhaLayer(16, kc, vc, 64, 256, 256, 0.0625)),
+                                16, 2048, 2048, 16, None, 16, 64, None)
+    assert st == built.DSA_ERR_WORKSPACE
