@@ -9,7 +9,7 @@
  *      ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
  *      Model, lightning-indexer bullet: a down-projected ReLU dot product summed
  *      with weights across heads; "DeepSeek Sparse Attention", In the code
- *      table: "ReLU(q.k) weighted sums", index_n_heads / index_head_dim).
+ *      table: ReLU(q.k) scores summed with weights, index_n_heads / index_head_dim).
  *   2. top-k: the k past tokens with the largest I[t, .]; when the causal
  *      context holds at most k tokens, all of them ("How GLM5.3 ...", Model,
  *      sparse-MLA bullet: top-k 2048, attention below 2K stays dense).  Equal
@@ -209,7 +209,7 @@ dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer,
 /*
  * The fused forward over compressed cache entries ("DeepSeek Sparse
  * Attention", In the code: the DeepSeek-V4 indexers score compressed KV
- * entries with ReLU(q.k) weighted sums and keep the top index_topk = 512 or
+ * entries with ReLU(q.k) scores summed with weights and keep the top index_topk = 512 or
  * 1024 entries for compressed sparse attention).  Each cache row (indexer key
  * and latent row alike) is one entry standing for compress_ratio consecutive
  * tokens: entry j of sequence b covers tokens compress_ratio * j .. + ratio - 1

@@ -3,7 +3,7 @@
 //   I[t, s] = sum_h w[t, h] * max(0, q_I[t, h, :] . k_I[s, :])
 // ("How GLM5.3 Sparse Attention Affects HBM Memory Usage", How it works /
 // Model, lightning-indexer bullet; "DeepSeek Sparse Attention", In the code:
-// ReLU(q.k) weighted sums).
+// the indexer sums ReLU(q.k) with weights).
 //
 // One work item = 128 consecutive keys of one sequence x one group of G
 // queries of that sequence.  The MMA puts the 128 keys on M (TMEM lanes) and

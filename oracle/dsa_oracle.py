@@ -16,7 +16,7 @@ What is computed, and where it is defined:
                       How it works / Model, first bullet (down-projected ReLU
                       dot product, summed with weights across heads; selection
                       shared by all attention heads); "DeepSeek Sparse
-                      Attention", In the code table ("ReLU(q.k) weighted sums").
+                      Attention", In the code table: the indexer sums ReLU(q.k) with weights).
   top-k selection     the k causal positions with the largest I[t, .]; when the
                       context holds at most k tokens every token is selected
                       ("How GLM5.3 ...", Model, second bullet: top-k 2048,
@@ -35,7 +35,7 @@ What is computed, and where it is defined:
                       for m consecutive tokens, with top-512 or top-1024
                       entries ("DeepSeek Sparse Attention", In the code: the
                       DeepSeek-V4 indexers score compressed KV entries with
-                      ReLU(q.k) weighted sums and keep index_topk = 512 or
+                      ReLU(q.k) scores summed with weights and keep index_topk = 512 or
                       1024).  Reading: entry j stands for tokens m j .. m j +
                       m - 1 and is visible to a query at position p once its
                       block is complete, so the query sees floor((p + 1) / m)
