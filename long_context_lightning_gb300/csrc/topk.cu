@@ -617,8 +617,13 @@ cudaError_t launch_topk(const TopkLaunch& a, cudaStream_t stream) {
   if (topk_cluster_cap() > 0) max_cluster = std::min(max_cluster, topk_cluster_cap());
   // cluster size: enough blocks per row that the rows fill a good share of the
   // GPU (each block reads less of the row), and chunks that fit the key cache
+  // fewest blocks per row whose chunks fit the key cache -- whole keys, or,
+  // when the rows outnumber what the GPU holds at once, the 16-bit key tops of
+  // chunks twice as long (more rows in flight beats faster rows then)
+  const bool many_rows = (int64_t)a.T * 2 > a.num_sms;
+  const int fit = many_rows ? 2 * kMaxCacheKeys : kMaxCacheKeys;
   int c = 1;
-  while (c < max_cluster && (a.max_n + c - 1) / c > kMaxCacheKeys) c *= 2;
+  while (c < max_cluster && (a.max_n + c - 1) / c > fit) c *= 2;
   while (c < max_cluster && (int64_t)a.T * c * 2 <= a.num_sms && (a.max_n + 2 * c - 1) / (2 * c) >= 4096) c *= 2;
   const int per = (((a.max_n + c - 1) / c) + 7) & ~7;
   // the cache holds whole keys, or the top 16 bits of each key of a chunk up to twice as long
