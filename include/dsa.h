@@ -228,6 +228,23 @@ dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_r
                                     size_t workspace_bytes, cudaStream_t stream, cudaEvent_t const* marks);
 
 /*
+ * dsa_forward for a serving step whose inputs arrive while it runs: the
+ * sparse-MLA launch waits for the caller's event `mla_ready` (recorded on
+ * another stream once the layers' queries are uploaded and their latent rows
+ * appended, so those copies overlap the indexer and the top-k), and
+ * `topk_done` is recorded on `stream` once idx is written (the caller may copy
+ * the index set back while the sparse MLA runs).  Either event may be NULL;
+ * both NULL is dsa_forward.  Events are the caller's (cudaEventDefault or
+ * cudaEventDisableTiming), and the call may be captured into a CUDA graph
+ * with the other stream forked from `stream`.  Tokens only (no compressed
+ * entries); everything else as dsa_forward.
+ */
+dsa_status_t dsa_forward_overlapped(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
+                                    int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                                    void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream, cudaEvent_t mla_ready, cudaEvent_t topk_done);
+
+/*
  * dsa_forward with timing marks: identical work, plus cudaEventRecord of the
  * caller's events on `stream` -- marks[0] before the first launch, marks[1]
  * after the per-call plan, marks[2] after the indexer, marks[3] after the
@@ -252,13 +269,14 @@ dsa_status_t dsa_forward_marked(const dsa_batch_t* batch, const dsa_indexer_t* i
  *   cache      the pool is WRITTEN (through cache->base): query token t of
  *              sequence b at position p_t goes to the row that holds token
  *              p_t of b; no other row changes.  A page id out of range is
- *              skipped and flagged DSA_ERR_BAD_INDEX.
- *   workspace  device, >= dsa_workspace_size(batch, 0) bytes.
+ *              skipped and flagged DSA_ERR_BAD_INDEX, and so is every token of a
+ *              sequence whose lengths break the dsa_batch_t rules.
+ * One launch, no workspace: each token's sequence is found on the device.
  * IndexShare: the index set dsa_forward writes is the group's stored top-k;
  * later layers of the group pass it to dsa_sparse_mla_fwd.
  */
 dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_t ld_rows, int32_t row_elems,
-                              const dsa_cache_t* cache, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                              const dsa_cache_t* cache, cudaStream_t stream);
 
 /*
  * HiSparse: HBM as a least-recently-used cache of one layer's latent rows over

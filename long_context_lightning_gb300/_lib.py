@@ -29,7 +29,7 @@ EXPORTS = ["dsa_status_string", "dsa_check_device_error", "dsa_workspace_size", 
            "dsa_selftest_timeout", "dsa_sparse_mla_fwd_noalloc", "dsa_selftest_topk_max_cluster", "dsa_cache_append",
            "dsa_forward_compressed", "dsa_hisparse_state_bytes", "dsa_hisparse_workspace_size", "dsa_hisparse_reset", "dsa_hisparse_fetch",
            "dsa_hisparse_resident", "dsa_hisparse_stats", "dsa_mha_project", "dsa_mha_workspace_size",
-           "dsa_sparse_mha_fwd", "dsa_selftest_topk_path"]
+           "dsa_sparse_mha_fwd", "dsa_selftest_topk_path", "dsa_forward_overlapped"]
 MHA_HEAD_DIM = 256
 NOALLOC_MAX_QUERIES = 4096
 
@@ -113,8 +113,11 @@ def load() -> ctypes.CDLL:
                                            POINTER(MlaLayer), c_void_p, c_int64, POINTER(c_void_p), POINTER(c_void_p),
                                            c_void_p, c_size_t, c_void_p, POINTER(c_void_p)]
     lib.dsa_cache_append.restype = c_int32
-    lib.dsa_cache_append.argtypes = [POINTER(Batch), c_void_p, c_int64, c_int32, POINTER(Cache), c_void_p, c_size_t,
-                                     c_void_p]
+    lib.dsa_cache_append.argtypes = [POINTER(Batch), c_void_p, c_int64, c_int32, POINTER(Cache), c_void_p]
+    lib.dsa_forward_overlapped.restype = c_int32
+    lib.dsa_forward_overlapped.argtypes = [POINTER(Batch), POINTER(Indexer), c_int32, c_int32, POINTER(MlaLayer),
+                                           c_void_p, c_int64, POINTER(c_void_p), POINTER(c_void_p), c_void_p,
+                                           c_size_t, c_void_p, c_void_p, c_void_p]
     lib.dsa_selftest_topk_max_cluster.restype = c_int32
     lib.dsa_selftest_topk_max_cluster.argtypes = [c_int32]
     lib.dsa_hisparse_state_bytes.restype = c_size_t
@@ -287,12 +290,34 @@ def forward_marked(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaL
            "dsa_forward_marked")
 
 
-def cache_append(batch: Batch, rows: torch.Tensor, cache: Cache, workspace: torch.Tensor, stream=None):
+def cache_append(batch: Batch, rows: torch.Tensor, cache: Cache, stream=None):
     """Write row t of `rows` (bf16 [T, >= row width]) into `cache` at query token t's position."""
     assert rows.dtype == torch.bfloat16 and rows.stride(1) == 1
     _check(load().dsa_cache_append(ctypes.byref(batch), _ptr(rows), rows.stride(0), rows.shape[1],
-                                   ctypes.byref(cache), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                   _stream(stream)), "dsa_cache_append")
+                                   ctypes.byref(cache), _stream(stream)), "dsa_cache_append")
+
+
+def _event(e):
+    if e is None:
+        return None
+    if not e.cuda_event:
+        raise ValueError("record each torch.cuda.Event once before passing it (torch creates it lazily)")
+    return e.cuda_event
+
+
+def forward_overlapped(batch: Batch, indexer: Indexer, k: int, layers: Sequence[MlaLayer], idx: torch.Tensor,
+                       outs: Sequence[torch.Tensor], lses, workspace: torch.Tensor, stream=None, mla_ready=None,
+                       topk_done=None):
+    """forward() whose sparse MLA waits for torch.cuda.Event `mla_ready` and which records
+    `topk_done` once idx is written (either may be None)."""
+    n = len(layers)
+    arr = (MlaLayer * n)(*layers)
+    out_ptrs = (c_void_p * n)(*[_ptr(o) for o in outs])
+    lse_ptrs = None if lses is None else (c_void_p * n)(*[_ptr(x) for x in lses])
+    _check(load().dsa_forward_overlapped(ctypes.byref(batch), ctypes.byref(indexer), k, n, arr, _ptr(idx),
+                                         idx.stride(0), out_ptrs, lse_ptrs, _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream),
+                                         _event(mla_ready), _event(topk_done)), "dsa_forward_overlapped")
 
 
 def hisparse_state_bytes(capacity: int, host_rows: int) -> int:

@@ -21,6 +21,8 @@ class SparseAttention:
     q_layers      per layer bf16 [T, H, D]; kv_pools per layer bf16 [rows, D]
     seq_start     int64 [B] (contiguous pools) or page_table int32 [B, P] (paged)
     compress_ratio  tokens per cache entry (pools of compressed entries; 1: one row per token)
+    idx, outs, lses  optional result buffers (int32 [T, topk]; per layer bf16 [T, H, d_v] and
+                  fp32 [T, H]); new ones are allocated when omitted
     """
 
     def __init__(self, cu_seqlens_q: torch.Tensor, seq_lens_k: torch.Tensor, q_idx: torch.Tensor,
@@ -28,7 +30,9 @@ class SparseAttention:
                  kv_pools: Sequence[torch.Tensor], d_v: int, scale: float, topk: int,
                  seq_start: Optional[torch.Tensor] = None, page_table: Optional[torch.Tensor] = None,
                  page_size: int = 64, total_q: Optional[int] = None, max_seqlen_k: Optional[int] = None,
-                 max_q_per_seq: Optional[int] = None, with_lse: bool = True, compress_ratio: int = 1):
+                 max_q_per_seq: Optional[int] = None, with_lse: bool = True, compress_ratio: int = 1,
+                 idx: Optional[torch.Tensor] = None, outs: Optional[Sequence[torch.Tensor]] = None,
+                 lses: Optional[Sequence[torch.Tensor]] = None):
         dev = q_idx.device
         self.topk = topk
         self.compress_ratio = compress_ratio
@@ -43,11 +47,17 @@ class SparseAttention:
                        for q, kv in zip(q_layers, kv_pools)]
         T = self.total_q
         H = q_layers[0].shape[1]
-        self.idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
-        self.outs: List[torch.Tensor] = [torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev)
-                                         for _ in q_layers]
-        self.lses: Optional[List[torch.Tensor]] = (
-            [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in q_layers] if with_lse else None)
+        # result buffers: the caller's (e.g. views of one staging buffer) or new ones
+        self.idx = torch.empty((T, topk), dtype=torch.int32, device=dev) if idx is None else idx
+        self.outs: List[torch.Tensor] = (
+            [torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev) for _ in q_layers] if outs is None
+            else list(outs))
+        if lses is not None:
+            self.lses: Optional[List[torch.Tensor]] = list(lses)
+        else:
+            self.lses = [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in q_layers] if with_lse else None
+        if tuple(self.idx.shape) != (T, topk) or self.idx.dtype != torch.int32 or len(self.outs) != len(q_layers):
+            raise ValueError("idx must be int32 [total_q, topk] and outs one [total_q, heads, d_v] per layer")
         ws = _lib.workspace_size(self.batch, topk)
         if ws == 0:
             raise ValueError("invalid batch description")
@@ -57,6 +67,16 @@ class SparseAttention:
         """indexer -> top-k -> sparse MLA for every layer; asynchronous on `stream`."""
         _lib.forward(self.batch, self.indexer, self.topk, self.layers, self.idx, self.outs, self.lses,
                      self.workspace, stream, compress_ratio=self.compress_ratio)
+        return self.idx, self.outs, self.lses
+
+    def forward_overlapped(self, stream=None, mla_ready=None, topk_done=None):
+        """forward() for a step whose layer inputs arrive while it runs: the sparse MLA waits
+        for torch.cuda.Event `mla_ready` (queries uploaded, latent rows appended on another
+        stream), and `topk_done` is recorded once the index set is written.  Tokens only."""
+        if self.compress_ratio != 1:
+            raise ValueError("forward_overlapped serves token caches (compress_ratio 1)")
+        _lib.forward_overlapped(self.batch, self.indexer, self.topk, self.layers, self.idx, self.outs, self.lses,
+                                self.workspace, stream, mla_ready, topk_done)
         return self.idx, self.outs, self.lses
 
     def scores_view(self) -> torch.Tensor:

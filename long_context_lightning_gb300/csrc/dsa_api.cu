@@ -185,9 +185,10 @@ dsa_status_t launch_topk_call(const dsa_batch_t* b, const float* scores, int64_t
 dsa_status_t launch_mla_call(const dsa_batch_t* b, int n_layers, const dsa_mla_layer_t* layers,
                              void* const* outs, float* const* lses, const int32_t* idx, int64_t ld_idx, int32_t k,
                              const PlanView& plan, const DeviceInfo& dev, cudaStream_t stream,
-                             bool plan_early = false, int ratio = 1) {
+                             bool plan_early = false, int ratio = 1, bool pdl = true) {
   MlaLaunch a;
   std::memset(&a, 0, sizeof(a));
+  a.pdl = pdl;
   for (int l = 0; l < n_layers; ++l) {
     a.layer[l].q = static_cast<const __nv_bfloat16*>(layers[l].q);
     a.layer[l].kv = view_of(layers[l].kv);
@@ -509,7 +510,8 @@ namespace {
 dsa_status_t forward_impl(const dsa_batch_t* batch, int ratio, const dsa_indexer_t* indexer, int32_t topk,
                           int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
                           void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
-                          cudaStream_t stream, cudaEvent_t const* marks) {
+                          cudaStream_t stream, cudaEvent_t const* marks, cudaEvent_t mla_ready = nullptr,
+                          cudaEvent_t topk_done = nullptr) {
   dsa_status_t s = check_batch(batch);
   if (s != DSA_OK) return s;
   if (ratio < 1 || ratio > batch->max_seqlen_k) return DSA_ERR_INVALID_ARG;
@@ -542,8 +544,12 @@ dsa_status_t forward_impl(const dsa_batch_t* batch, int ratio, const dsa_indexer
   if ((s = launch_topk_call(batch, scores, ld, topk, idx, ld_idx, plan, dev, stream, true, ratio)) != DSA_OK)
     return s;
   if (!mark(3)) return DSA_ERR_CUDA;
+  if (topk_done != nullptr && cudaEventRecord(topk_done, stream) != cudaSuccess) return DSA_ERR_CUDA;
+  if (mla_ready != nullptr && cudaStreamWaitEvent(stream, mla_ready, 0) != cudaSuccess) return DSA_ERR_CUDA;
+  // a launch that also waits on the caller's event is an ordinary one: a
+  // programmatic edge may not join another stream's work in a captured graph
   if ((s = launch_mla_call(batch, n_layers, layers, outs, lses, idx, ld_idx, topk, plan, dev, stream, true,
-                           ratio)) != DSA_OK)
+                           ratio, mla_ready == nullptr)) != DSA_OK)
     return s;
   return mark(4) ? DSA_OK : DSA_ERR_CUDA;
 }
@@ -566,6 +572,14 @@ dsa_status_t dsa_forward_compressed(const dsa_batch_t* batch, int32_t compress_r
                                     size_t workspace_bytes, cudaStream_t stream, cudaEvent_t const* marks) {
   return forward_impl(batch, compress_ratio, indexer, topk, n_layers, layers, idx, ld_idx, outs, lses, workspace,
                       workspace_bytes, stream, marks);
+}
+
+dsa_status_t dsa_forward_overlapped(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,
+                                    int32_t n_layers, const dsa_mla_layer_t* layers, int32_t* idx, int64_t ld_idx,
+                                    void* const* outs, float* const* lses, void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream, cudaEvent_t mla_ready, cudaEvent_t topk_done) {
+  return forward_impl(batch, 1, indexer, topk, n_layers, layers, idx, ld_idx, outs, lses, workspace,
+                      workspace_bytes, stream, nullptr, mla_ready, topk_done);
 }
 
 dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk, int32_t n_layers,
@@ -645,27 +659,25 @@ dsa_status_t dsa_selftest_mma(const void* a, const void* b, float* d, int32_t a_
 }
 
 dsa_status_t dsa_cache_append(const dsa_batch_t* batch, const void* rows, int64_t ld_rows, int32_t row_elems,
-                              const dsa_cache_t* cache, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+                              const dsa_cache_t* cache, cudaStream_t stream) {
   dsa_status_t s = check_batch(batch);
   if (s != DSA_OK) return s;
   if (cache == nullptr || rows == nullptr || !aligned16(rows)) return DSA_ERR_INVALID_ARG;
   if (row_elems < 8 || row_elems % 8 != 0 || ld_rows < row_elems || ld_rows % 8 != 0) return DSA_ERR_INVALID_ARG;
   if ((s = check_cache(*cache, row_elems, batch->max_seqlen_k)) != DSA_OK) return s;
-  if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < plan_bytes(batch->total_q))
-    return DSA_ERR_WORKSPACE;
   if (batch->total_q == 0) return DSA_OK;
   DeviceInfo dev;
   if (device_info(&dev) != DSA_OK) return DSA_ERR_CUDA;
-  PlanView plan;
-  if ((s = run_plan(batch, 1, 0, workspace, dev, stream, &plan)) != DSA_OK) return s;
   AppendLaunch a;
   a.src = rows;
   a.ld_src = ld_rows;
   a.c = view_of(*cache);
   a.row_elems = row_elems;
   a.T = batch->total_q;
-  a.q_seq = plan.q_seq;
-  a.q_n = plan.q_n;
+  a.B = batch->num_seqs;
+  a.max_seqlen_k = batch->max_seqlen_k;
+  a.cu_seqlens_q = batch->cu_seqlens_q;
+  a.seq_lens_k = batch->seq_lens_k;
   a.err = dev.err;
   return launch_cache_append(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }

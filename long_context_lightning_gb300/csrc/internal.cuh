@@ -156,6 +156,7 @@ struct MlaLaunch {
   int* err;
   int num_sms;
   bool plan_early = false;  // as in TopkLaunch
+  bool pdl = true;          // programmatic launch after the top-k (off when the stream also waits on an event)
 };
 cudaError_t launch_sparse_mla(const MlaLaunch& a, cudaStream_t stream);
 
@@ -165,8 +166,10 @@ struct AppendLaunch {
   CacheView c;
   int32_t row_elems;  // multiple of 8
   int32_t T;
-  const int32_t* q_seq;
-  const int32_t* q_n;
+  int32_t B;
+  int32_t max_seqlen_k;
+  const int32_t* cu_seqlens_q;  // device [B + 1]
+  const int32_t* seq_lens_k;    // device [B]
   int* err;
 };
 cudaError_t launch_cache_append(const AppendLaunch& a, cudaStream_t stream);

@@ -737,7 +737,7 @@ cudaError_t launch_t(const MlaLaunch& a, cudaStream_t stream, int which) {
   at[0].val.clusterDim.z = 1;
   at[1] = pdl_attribute();
   cfg.attrs = at;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = a.pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, tq[0], tq[1], tq[2], tq[3], tc[0], tc[1], tc[2], tc[3], p);
 }
 

@@ -123,9 +123,16 @@ def test_host_validation_of_the_later_entry_points(built):
                                         None, 16, 1 << 30, None, None)
         assert st == built.DSA_ERR_INVALID_ARG
     # cache append: no cache, odd row width
-    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 576, None, 16, 1 << 20, None) == built.DSA_ERR_INVALID_ARG
-    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 570, ctypes.byref(cache), 16, 1 << 20,
-                                None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 576, None, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_append(ctypes.byref(b), 16, 576, 570, ctypes.byref(cache), None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_cache_append(ctypes.byref(b), 8, 576, 576, ctypes.byref(cache), None) == built.DSA_ERR_INVALID_ARG
+    # overlapped forward: the same checks as dsa_forward, before any event is touched
+    assert lib.dsa_forward_overlapped(ctypes.byref(b), ctypes.byref(ix), 0, 1, arr, 16, 2048, outs, None, 16,
+                                      1 << 30, None, None, None) == built.DSA_ERR_UNSUPPORTED
+    assert lib.dsa_forward_overlapped(ctypes.byref(b), ctypes.byref(ix), 2048, 0, arr, 16, 2048, outs, None, 16,
+                                      1 << 30, None, None, None) == built.DSA_ERR_INVALID_ARG
+    assert lib.dsa_forward_overlapped(ctypes.byref(b), ctypes.byref(ix), 2048, 1, arr, 16, 2048, outs, None, 16,
+                                      16, None, None, None) == built.DSA_ERR_WORKSPACE
     # HiSparse sizing and argument checks
     assert lib.dsa_hisparse_state_bytes(0, 100) == 0 and lib.dsa_hisparse_state_bytes(16, 0) == 0
     assert lib.dsa_hisparse_state_bytes(16, 100) >= 12 * 100 + 24 * 16
