@@ -182,12 +182,13 @@ def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: fl
 # hex digits of the sha256 of the kernel's source file when it was captured.
 # A source that has changed since makes the figure stale: it is reported as
 # null.  Captured with
-#   ncu --set full --clock-control none -k regex:<kernel>_kernel -s 2 -c 1 \
+#   ncu --set full --clock-control none \
+#       -k regex:"indexer_kernel|topk_kernel|sparse_mla_kernel" -s 3 -c 3 \
 #       -o <report> python bench.py --steps 5 --warmup 3 --no-per-config
 NCU_TRAFFIC = {
-    ("decode", "indexer"): ("indexer.cu", "9168a47dab63d1da", 275455488.0),
-    ("decode", "topk"): ("topk.cu", "dfb51a1062365d6c", 4273664.0),
-    ("decode", "sparse_mla"): ("sparse_mla.cu", "1a5e7a3244462a12", 82912512.0),
+    ("decode", "indexer"): ("indexer.cu", "b318cf7c994a392b", 275874048.0),
+    ("decode", "topk"): ("topk.cu", "51834c3a49681375", 4273664.0),
+    ("decode", "sparse_mla"): ("sparse_mla.cu", "73585f896bfb16d3", 82764800.0),
 }
 
 
