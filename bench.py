@@ -309,6 +309,19 @@ class _Run:
             raise RuntimeError(f"{what}: device error: {_lib.status_string(status)}")
 
 
+# nominal GB300 figures, reported beside the measured-peak fractions: HBM3e
+# bandwidth (about 8 TB/s) and the dense bf16 tensor rate
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def _with_nominal(roof):
+    nominal = NOMINAL_HBM_GBS if roof["unit"] == "GB/s" else NOMINAL_BF16_TFLOPS
+    roof["nominal_peak"] = nominal
+    roof["frac_of_nominal"] = roof["achieved"] / nominal
+    return roof
+
+
 def _roofline(wl, kern_ms, peaks, workload):
     """Dominant kernel's roofline (HBM bytes or tensor FLOPs, algorithmic), plus the sparse MLA's and the
     whole step's byte fractions."""
@@ -339,7 +352,7 @@ def _roofline(wl, kern_ms, peaks, workload):
     mla = {"bound": "hbm", "achieved": mla_gbs, "peak": hbm, "unit": "GB/s", "frac": mla_gbs / hbm,
            "traffic": _traffic(workload, "sparse_mla"), "algorithmic_bytes_per_launch": mla_b,
            "tflops": mla_f / (kern_ms["sparse_mla"] * 1e-3) / 1e12}
-    return roof, mla, A.forward_bytes(shp), A.forward_flops(shp)
+    return _with_nominal(roof), _with_nominal(mla), A.forward_bytes(shp), A.forward_flops(shp)
 
 
 def _oracle_sample(wl, queries, kv_on_device=False, min_s=2.0):
@@ -529,10 +542,10 @@ def run_gpu(args, rank, world, local_rank):
                              "launching stream, L2 flushed before each call; the events stop programmatic "
                              "overlap, so the four means add up to more than ms_per_step",
         "sparse_mla_roofline": mla_roof,
-        "step_roofline": {"bound": "hbm", "achieved": all_bytes / (total_ms / args.steps * 1e-3) / 1e9,
-                          "peak": hbm, "unit": "GB/s",
-                          "frac": all_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm,
-                          "algorithmic_bytes_per_step": all_bytes},
+        "step_roofline": _with_nominal({"bound": "hbm", "achieved": all_bytes / (total_ms / args.steps * 1e-3) / 1e9,
+                                        "peak": hbm, "unit": "GB/s",
+                                        "frac": all_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm,
+                                        "algorithmic_bytes_per_step": all_bytes}),
         "e2e": {"value": T * world / (e2e_ms / 1e3), "unit": "query tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "step": "h2d of the step's indexer inputs, lengths and new indexer keys (one pinned buffer) -> "
@@ -787,11 +800,11 @@ def _mha_config(args, dev, stream, flush_l2, peaks):
                     f"192 up-projected + 64 rope dims, values 256 up-projected, from the 576-dim latent",
         "value": T / (ms * 1e-3), "unit": "query tokens/s", "ms_per_step": ms, "steps": steps,
         "kernels_ms": kern_ms,
-        "roofline": {"bound": "tensor", "kernel": "mha_attend", "achieved": att_tf, "peak": tf_sust,
-                     "unit": "TFLOP/s", "frac": att_tf / tf_sust, "traffic": None,
-                     "peak_kind": f"{kind} (bf16 sustained)", "algorithmic_flops_per_launch": att_f,
-                     "executed_flops_per_launch": exec_f,
-                     "executed_tflops": exec_f / (kern_ms["mha_attend"] * 1e-3) / 1e12},
+        "roofline": _with_nominal({"bound": "tensor", "kernel": "mha_attend", "achieved": att_tf, "peak": tf_sust,
+                                   "unit": "TFLOP/s", "frac": att_tf / tf_sust, "traffic": None,
+                                   "peak_kind": f"{kind} (bf16 sustained)", "algorithmic_flops_per_launch": att_f,
+                                   "executed_flops_per_launch": exec_f,
+                                   "executed_tflops": exec_f / (kern_ms["mha_attend"] * 1e-3) / 1e12}),
         "mha_project": {"tflops": proj_tf, "frac": proj_tf / tf_sust, "flops_per_launch": proj_f},
         "cpu_baseline": {"value": done / dt, "unit": "query tokens/s", "kind": "oracle",
                          "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
