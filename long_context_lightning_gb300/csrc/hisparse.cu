@@ -151,13 +151,57 @@ __device__ __forceinline__ int64_t entry_row(const HsParams& p, int f, bool flag
   return row;
 }
 
-// Entry f's status in this step: 1 = first request of a missing row, 2 =
-// first request of a resident row, 0 = anything else.
-__device__ __forceinline__ int entry_kind(const HsParams& p, int f, uint32_t step, int64_t* row_out) {
-  const int64_t row = entry_row(p, f, false);
-  *row_out = row;
-  if (row < 0 || p.s.claim[row] != claim_key(step, (uint32_t)f)) return 0;
-  return p.s.slot_of_row[row] < 0 ? 1 : 2;
+// Status of the kPer selection entries f0 .. f0 + kPer - 1 in this step:
+// kind 1 = first request of a missing row, 2 = first request of a resident
+// row, 0 = anything else (past the selection: kind 0, row -1).  Every load step is issued for all entries at once --
+// context lengths, sequences and positions, then pool rows, then claims, then
+// slots -- with indices clamped into range and the conditions applied after,
+// so a thread waits four load latencies, not four per entry.
+__device__ __forceinline__ void entry_kinds(const HsParams& p, int f0, uint32_t step, int64_t (&rows)[kPer],
+                                            int (&kinds)[kPer]) {
+  const int n_entries = p.T * p.k;
+  int n_t[kPer], seq[kPer], pos[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int f = min(f0 + i, n_entries - 1);
+    const int t = f / p.k, j = f - t * p.k;
+    n_t[i] = __ldg(p.q_n + t);
+    seq[i] = __ldg(p.q_seq + t);
+    pos[i] = __ldg(p.idx + (int64_t)t * p.ld_idx + j);
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int f = f0 + i;
+    const int j = f - (min(f, n_entries - 1) / p.k) * p.k;
+    const bool ok = f < n_entries && j < min(n_t[i], p.k) && pos[i] >= 0 && pos[i] < n_t[i];
+    const int64_t row = cache_row(p.host, seq[i], ok ? pos[i] : 0);
+    rows[i] = (ok && row >= 0 && row < p.host_rows) ? row : -1;
+  }
+  uint64_t claim[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) claim[i] = rows[i] >= 0 ? p.s.claim[rows[i]] : 0ull;
+  int slot[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const bool first = rows[i] >= 0 && claim[i] == claim_key(step, (uint32_t)(f0 + i));
+    slot[i] = first ? p.s.slot_of_row[rows[i]] : 0;
+    kinds[i] = first ? (slot[i] < 0 ? 1 : 2) : 0;
+  }
+}
+
+// The kPer positions i0 .. i0 + kPer - 1 of an LRU order (two 16-byte loads;
+// past the capacity: -2).
+__device__ __forceinline__ void lru_slots(const int32_t* lru, int i0, int cap, int (&slots)[kPer]) {
+  static_assert(kPer == 8, "two 16-byte loads per thread");
+  if (i0 + kPer <= cap) {
+    const int4 v0 = *reinterpret_cast<const int4*>(lru + i0);
+    const int4 v1 = *reinterpret_cast<const int4*>(lru + i0 + 4);
+    slots[0] = v0.x, slots[1] = v0.y, slots[2] = v0.z, slots[3] = v0.w;
+    slots[4] = v1.x, slots[5] = v1.y, slots[6] = v1.z, slots[7] = v1.w;
+  } else {
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) slots[i] = i0 + i < cap ? lru[i0 + i] : -2;
+  }
 }
 
 // Exclusive block-wide scan of one int per thread (all threads call it).
@@ -223,12 +267,15 @@ __global__ void __launch_bounds__(kThreads) hs_count_kernel(HsParams p) {
   if ((int)blockIdx.x < p.n_entry_chunks) {
     int miss = 0, hit = 0;
     const int f0 = blockIdx.x * kChunk + threadIdx.x * kPer;
-    for (int i = 0; i < kPer; ++i) {
-      if (f0 + i >= n_entries) break;
-      int64_t row;
-      const int kind = entry_kind(p, f0 + i, step, &row);
-      miss += kind == 1;
-      hit += kind == 2;
+    if (f0 < n_entries) {
+      int64_t rows[kPer];
+      int kinds[kPer];
+      entry_kinds(p, f0, step, rows, kinds);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        miss += kinds[i] == 1;
+        hit += kinds[i] == 2;
+      }
     }
     int tot_m, tot_h;
     scan_block(miss, warp_sums, &tot_m);
@@ -242,14 +289,17 @@ __global__ void __launch_bounds__(kThreads) hs_count_kernel(HsParams p) {
     const int32_t* lru = p.s.lru[p.s.stats[ST_PARITY] & 1];
     int a = 0;
     const int i0 = chunk * kChunk + threadIdx.x * kPer;
-    for (int i = 0; i < kPer; ++i) {
-      if (i0 + i >= p.capacity) break;
-      const int slot = lru[i0 + i];
-      if ((unsigned)slot >= (unsigned)p.capacity) {  // the order is a permutation of the slots
-        atomicOr(p.err, DEV_ERR_BAD_INDEX);
-        continue;
+    if (i0 < p.capacity) {
+      int slots[kPer];
+      lru_slots(lru, i0, p.capacity, slots);
+      bool bad = false;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const bool in = (unsigned)slots[i] < (unsigned)p.capacity;
+        bad |= !in && slots[i] != -2;  // the order is a permutation of the slots
+        a += in && p.s.used[in ? slots[i] : 0] != (int32_t)step;
       }
-      a += p.s.used[slot] != (int32_t)step;
+      if (bad) atomicOr(p.err, DEV_ERR_BAD_INDEX);
     }
     int tot;
     scan_block(a, warp_sums, &tot);
@@ -313,9 +363,10 @@ __global__ void __launch_bounds__(kThreads) hs_scatter_kernel(HsParams p) {
     for (int i = 0; i < kPer; ++i) {
       kinds[i] = 0;
       rows[i] = -1;
-      if (f0 + i < n_entries) kinds[i] = entry_kind(p, f0 + i, step, &rows[i]);
-      miss += kinds[i] == 1;
     }
+    if (f0 < n_entries) entry_kinds(p, f0, step, rows, kinds);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) miss += kinds[i] == 1;
     int tot;
     int pos = p.c.miss[blockIdx.x] + scan_block(miss, warp_sums, &tot);
 #pragma unroll
@@ -331,16 +382,12 @@ __global__ void __launch_bounds__(kThreads) hs_scatter_kernel(HsParams p) {
     int a = 0;
     const int i0 = chunk * kChunk + threadIdx.x * kPer;
 #pragma unroll
+    for (int i = 0; i < kPer; ++i) slots[i] = -1;
+    if (i0 < cap) lru_slots(lru, i0, cap, slots);
+#pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      slots[i] = -1;
-      is_a[i] = 0;
-      if (i0 + i < cap) {
-        const int slot = lru[i0 + i];
-        if ((unsigned)slot < (unsigned)cap) {
-          slots[i] = slot;
-          is_a[i] = p.s.used[slot] != (int32_t)step;
-        }
-      }
+      if ((unsigned)slots[i] >= (unsigned)cap) slots[i] = -1;
+      is_a[i] = slots[i] >= 0 && p.s.used[slots[i] >= 0 ? slots[i] : 0] != (int32_t)step;
       a += is_a[i];
     }
     int tot;
