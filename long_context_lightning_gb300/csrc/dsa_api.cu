@@ -156,6 +156,7 @@ dsa_status_t launch_indexer_call(const dsa_batch_t* b, const dsa_indexer_t* ix, 
   a.d = ix->head_dim;
   a.T = b->total_q;
   a.group = indexer_group(b);
+  a.keys_once = b->max_q_per_seq <= a.group;
   a.scores = scores;
   a.ld = ld;
   a.plan = plan;

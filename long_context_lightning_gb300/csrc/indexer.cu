@@ -67,6 +67,8 @@ struct IdxParams {
   int64_t ld;
   PlanView plan;
   int* err;
+  int32_t keys_once;  // key tiles are read once: they enter L2 as evict-first, so the
+                      // scores written meanwhile stay there for the top-k
 };
 
 // Work item -> group: the last g with start[g] <= item (start is non-decreasing,
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(IdxCfg<KB, NH, G>::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && w0 < w1) {
+      const uint64_t once = l2_policy_evict_first();
       int stage = 0;
       uint32_t phase = 0;
       int g = g_first;
@@ -192,7 +195,12 @@ __global__ void __launch_bounds__(IdxCfg<KB, NH, G>::THREADS, 1)
         if (!p.k.paged) {
           const int64_t row0 = __ldg(p.k.seq_start + b) + (int64_t)kt * 128;
           mbar_arrive_expect_tx(bar_a_full(stage), C::A_BYTES);
-          for (int kb = 0; kb < KB; ++kb) tma_load_2d(dst + kb * 128 * 128, &tm_k, bar_a_full(stage), kb * 64, (int32_t)row0);
+          for (int kb = 0; kb < KB; ++kb) {
+            if (p.keys_once)
+              tma_load_2d_hint(dst + kb * 128 * 128, &tm_k, bar_a_full(stage), kb * 64, (int32_t)row0, once);
+            else
+              tma_load_2d(dst + kb * 128 * 128, &tm_k, bar_a_full(stage), kb * 64, (int32_t)row0);
+          }
         } else {
           // two 64-token pages per tile; pages past the sequence are not read
           const int n_pages = (gi.w + p.k.page_size - 1) / p.k.page_size;
@@ -210,8 +218,14 @@ __global__ void __launch_bounds__(IdxCfg<KB, NH, G>::THREADS, 1)
           mbar_arrive_expect_tx(bar_a_full(stage), valid * KB * 64 * 128);
           for (int h = 0; h < 2; ++h) {
             if (phys[h] < 0) continue;
-            for (int kb = 0; kb < KB; ++kb)
-              tma_load_2d(dst + kb * 128 * 128 + h * 64 * 128, &tm_k, bar_a_full(stage), kb * 64, (int32_t)(phys[h] * 64));
+            for (int kb = 0; kb < KB; ++kb) {
+              if (p.keys_once)
+                tma_load_2d_hint(dst + kb * 128 * 128 + h * 64 * 128, &tm_k, bar_a_full(stage), kb * 64,
+                                 (int32_t)(phys[h] * 64), once);
+              else
+                tma_load_2d(dst + kb * 128 * 128 + h * 64 * 128, &tm_k, bar_a_full(stage), kb * 64,
+                            (int32_t)(phys[h] * 64));
+            }
           }
         }
         pend[stage] = (int)phase;
@@ -370,6 +384,7 @@ cudaError_t launch_t(const IndexerLaunch& a, cudaStream_t stream) {
   p.ld = a.ld;
   p.plan = a.plan;
   p.err = a.err;
+  p.keys_once = a.keys_once ? 1 : 0;
   cudaError_t e = cudaFuncSetAttribute(indexer_kernel<KB, NH, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -108,6 +108,7 @@ struct IndexerLaunch {
   int32_t d;
   int32_t T;
   int32_t group;      // G
+  bool keys_once;     // every sequence is one query group: each key tile is read once
   float* scores;
   int64_t ld;
   PlanView plan;
