@@ -186,7 +186,7 @@ def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: fl
 #       -k regex:"indexer_kernel|topk_kernel|sparse_mla_kernel" -s 3 -c 3 \
 #       -o <report> python bench.py --steps 5 --warmup 3 --no-per-config
 NCU_TRAFFIC = {
-    ("decode", "indexer"): ("indexer.cu", "b318cf7c994a392b", 275874048.0),
+    ("decode", "indexer"): ("indexer.cu", "5f358bf61f8aaa44", 273867264.0),
     ("decode", "topk"): ("topk.cu", "51834c3a49681375", 4273664.0),
     ("decode", "sparse_mla"): ("sparse_mla.cu", "73585f896bfb16d3", 82764800.0),
 }
