@@ -179,3 +179,26 @@ def test_host_validation_of_the_later_entry_points(built):
     st = lib.dsa_sparse_mha_fwd(ctypes.byref(b), ctypes.byref(built.MhaLayer(16, kc, vc, 64, 256, 256, 0.0625)),
                                 16, 2048, 2048, 16, None, 16, 64, None)
     assert st == built.DSA_ERR_WORKSPACE
+
+
+def test_sparse_attention_result_buffers_checked_without_gpu(built):
+    # caller-supplied result buffers must have the call's shapes; the check is
+    # host-side, before any launch (the tensors here are on the CPU)
+    import torch
+    import dsa_workloads as W
+    from long_context_lightning_gb300 import SparseAttention
+    spec = W.SPECS["tiny"]
+    wl = W.make_workload(spec)
+
+    def make(**kw):
+        return SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, spec.d_v,
+                               spec.scale, spec.topk, seq_start=wl.seq_start, **kw)
+    T = wl.total_q
+    ok = make(idx=torch.empty((T, spec.topk), dtype=torch.int32))
+    assert ok.idx.shape == (T, spec.topk)
+    with pytest.raises(ValueError):
+        make(idx=torch.empty((T, spec.topk + 1), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        make(idx=torch.empty((T, spec.topk), dtype=torch.int64))
+    with pytest.raises(ValueError):
+        make(outs=[])
