@@ -58,9 +58,9 @@ def _worker(rank, world, port, out):
 def test_two_cpu_ranks_run_their_own_batches_and_aggregate():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    ctx = mp.get_context("spawn")  # no fork of this (threaded) test process, the manager's included
+    mgr = ctx.Manager()
     out = mgr.dict()
-    ctx = mp.get_context("spawn")
     procs = [ctx.Process(target=_worker, args=(r, world, port, out)) for r in range(world)]
     for p in procs:
         p.start()
