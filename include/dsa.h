@@ -170,6 +170,8 @@ dsa_status_t dsa_indexer_scores(const dsa_batch_t* batch, const dsa_indexer_t* i
  * entries s < n_t are read).  Writes idx[t * ld_idx + j], j < topk: the
  * selected positions in ascending order, then -1 padding when n_t < topk.
  * topk in 1..2048.
+ *   workspace  device, >= dsa_workspace_size(batch, 0) bytes (the per-call
+ *              plan; the score matrix's share of that size is not used here).
  */
 dsa_status_t dsa_topk(const dsa_batch_t* batch, const float* scores, int64_t ld_scores, int32_t topk,
                       int32_t* idx, int64_t ld_idx, void* workspace, size_t workspace_bytes,
