@@ -202,3 +202,22 @@ def test_sparse_attention_result_buffers_checked_without_gpu(built):
         make(idx=torch.empty((T, spec.topk), dtype=torch.int64))
     with pytest.raises(ValueError):
         make(outs=[])
+
+
+def test_header_is_plain_c_and_links(built, tmp_path):
+    # a C99 program against include/dsa.h, linked to the built libdsa.so,
+    # calls the host-side entry points without a GPU
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if gcc is None or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers are not available")
+    lib_dir = os.path.dirname(built.load()._name)
+    exe = str(tmp_path / "c_abi_check")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc,
+                        os.path.join(ROOT, "tests", "c_abi_check.c"), "-o", exe, "-L", lib_dir, "-ldsa",
+                        "-Wl,-rpath," + lib_dir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
