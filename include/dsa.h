@@ -387,7 +387,7 @@ typedef struct {
   int32_t n_heads;      /* 1 .. DSA_MHA_MAX_HEADS */
   int32_t head_dim;     /* DSA_MHA_HEAD_DIM */
   int32_t v_head_dim;   /* DSA_MHA_HEAD_DIM */
-  float scale;          /* softmax scale, e.g. 1/sqrt(256) */
+  float scale;          /* softmax scale, > 0 (else DSA_ERR_INVALID_ARG), e.g. 1/sqrt(256) */
 } dsa_mha_layer_t;
 
 /* Workspace bytes of dsa_sparse_mha_fwd (the per-call plan and one selection

@@ -819,6 +819,7 @@ dsa_status_t dsa_sparse_mha_fwd(const dsa_batch_t* batch, const dsa_mha_layer_t*
   if (layer == nullptr || layer->q == nullptr || !aligned16(layer->q)) return DSA_ERR_INVALID_ARG;
   if (layer->head_dim != DSA_MHA_HEAD_DIM || layer->v_head_dim != DSA_MHA_HEAD_DIM) return DSA_ERR_UNSUPPORTED;
   if (layer->n_heads < 1 || layer->n_heads > DSA_MHA_MAX_HEADS) return DSA_ERR_UNSUPPORTED;
+  if (!(layer->scale > 0.f)) return DSA_ERR_INVALID_ARG;  // a softmax scale: positive (and not NaN)
   if (batch->max_seqlen_k > DSA_MHA_MAX_CONTEXT) return DSA_ERR_UNSUPPORTED;
   const dsa_cache_t& kc = layer->k;
   const dsa_cache_t& vc = layer->v;

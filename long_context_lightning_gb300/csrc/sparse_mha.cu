@@ -485,17 +485,14 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       mbar_arrive(s_free(u));
       // the maximum over all 64 keys (both threads of the row find the same),
       // the exponentials for this thread's 32
-      float mt = neg_inf();
+      // of the raw selected scores, scaled once: the scale is positive, so
+      // max(s) * scale = max(s * scale) under rounding as well
+      float mr = neg_inf();
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const uint32_t bit = ((c < 32 ? bits.x : bits.y) >> (c & 31)) & 1u;
-        if (bit) mt = fmaxf(mt, __uint_as_float(sv[c]) * p.scale_log2);
-      }
+      for (int c = 0; c < 64; ++c)
+        mr = fmaxf(mr, ((c < 32 ? bits.x : bits.y) & (1u << (c & 31))) ? __uint_as_float(sv[c]) : neg_inf());
+      const float mt = mr * p.scale_log2;
       const uint32_t mine = hf ? bits.y : bits.x;
-      float x[32];
-#pragma unroll
-      for (int c = 0; c < 32; ++c)
-        x[c] = ((mine >> c) & 1u) ? __uint_as_float(hf ? sv[32 + c] : sv[c]) * p.scale_log2 : neg_inf();
       // the reference moves when a score passes it by more than 2^8; O and l
       // follow it (TMEM loads and stores are warp-wide: a row that keeps its
       // reference is scaled by 1).  Rescaling O needs the previous P.V done.
@@ -522,10 +519,12 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       if (move) m_ref = mt;
       uint32_t pk[16];
       float lsum = 0.f;
+      // p = 2^(s * scale - m_ref) for this thread's selected keys, one FMA each
 #pragma unroll
       for (int c = 0; c < 32; c += 2) {
-        const float p0 = x[c] == neg_inf() ? 0.f : ex2_approx(x[c] - m_ref);
-        const float p1 = x[c + 1] == neg_inf() ? 0.f : ex2_approx(x[c + 1] - m_ref);
+        const float s0 = __uint_as_float(hf ? sv[32 + c] : sv[c]), s1 = __uint_as_float(hf ? sv[33 + c] : sv[c + 1]);
+        const float p0 = (mine & (1u << c)) ? ex2_approx(fmaf(s0, p.scale_log2, -m_ref)) : 0.f;
+        const float p1 = (mine & (1u << (c + 1))) ? ex2_approx(fmaf(s1, p.scale_log2, -m_ref)) : 0.f;
         const uint32_t w = pack_bf16x2(p0, p1);
         lsum += bf16lo_to_f32(w) + bf16hi_to_f32(w);
         pk[c >> 1] = w;
