@@ -437,25 +437,37 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
         bad |= !mbar_wait(bar_s_full, par, abort_flag, p.err);
         tc_fence_after();
         const bool kv = valid_s[srow] != 0;
-        float x[32];
+        uint32_t r[32];  // this key's raw scores for heads h0..h0+31
         auto load_scores = [&]() {
-          uint32_t r[32];
           tmem_ld32(lane_base + C::S_COL + h0, r);
           tmem_wait_ld();
+        };
+        // d = score x scale - the head's reference (log2 units), one FMA each:
+        // it decides the overflow vote and gives the probability 2^d
+        float d[32];
+        auto diffs = [&]() {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) x[i] = kv ? __uint_as_float(r[i]) * c : -INFINITY;
+          for (int i = 0; i < 32; i += 4) {
+            const float4 m4 = *reinterpret_cast<const float4*>(mref_s + h0 + i);
+            d[i] = fmaf(__uint_as_float(r[i]), c, -m4.x);
+            d[i + 1] = fmaf(__uint_as_float(r[i + 1]), c, -m4.y);
+            d[i + 2] = fmaf(__uint_as_float(r[i + 2]), c, -m4.z);
+            d[i + 3] = fmaf(__uint_as_float(r[i + 3]), c, -m4.w);
+          }
         };
         load_scores();
+        diffs();
         bool over = false;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 m4 = *reinterpret_cast<const float4*>(mref_s + h0 + i);
-          over |= (x[i] > m4.x + kRescaleLog2) | (x[i + 1] > m4.y + kRescaleLog2) | (x[i + 2] > m4.z + kRescaleLog2) |
-                  (x[i + 3] > m4.w + kRescaleLog2);
-        }
-        if (bar_red_or(4, kSoftmaxThreads, over)) {
+        for (int i = 0; i < 32; ++i) over |= d[i] > kRescaleLog2;
+        if (bar_red_or(4, kSoftmaxThreads, kv && over)) {
           // move the reference of every head whose tile max passed it
-          red_s[quad * 64 + h0 + lane] = transpose_reduce32<true>(x, lane);
+          {
+            float x[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = kv ? __uint_as_float(r[i]) * c : -INFINITY;
+            red_s[quad * 64 + h0 + lane] = transpose_reduce32<true>(x, lane);
+          }
           named_bar_sync(3, kSoftmaxThreads);
           bool rescale = false;
           if (st < 64) {
@@ -484,30 +496,28 @@ __global__ void __launch_bounds__(kProducerThreads + 32 + kSoftmaxThreads, 1)
               for (int q = 0; q < 2 * MB; ++q) {  // 16 columns at a time keeps the registers low
                 const uint32_t col = lane_base + (q >> 1) * 64 + h0 + (q & 1) * 16;
                 const float* a = alpha_s + h0 + (q & 1) * 16;
-                uint32_t r[16];
-                tmem_ld16(col, r);
+                uint32_t o[16];
+                tmem_ld16(col, o);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * a[i]);
-                tmem_st16(col, r);
+                for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * a[i]);
+                tmem_st16(col, o);
               }
               tmem_wait_st();
             }
           }
           load_scores();  // reloaded rather than kept live across the rescale
+          diffs();        // against the moved references
         }
         // probabilities, running sums, this key's P^T row for heads h0..h0+31 (bf16)
         const uint32_t prow = sbase + C::OFF_KV + (NB - 1) * kBlk + srow * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           float pv[8];
-          const float4 ma = *reinterpret_cast<const float4*>(mref_s + h0 + cc * 8);
-          const float4 mb4 = *reinterpret_cast<const float4*>(mref_s + h0 + cc * 8 + 4);
-          const float mref[8] = {ma.x, ma.y, ma.z, ma.w, mb4.x, mb4.y, mb4.z, mb4.w};
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const int i = cc * 8 + j;
-            pv[j] = x[i] == -INFINITY ? 0.f : ex2_approx(x[i] - mref[j]);
+            pv[j] = kv ? ex2_approx(d[i]) : 0.f;
             lsum[i] += pv[j];
           }
           const int chunk = half * 4 + cc;
