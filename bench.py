@@ -182,13 +182,13 @@ def job_throughput(units_per_rank: int, world: int, steps: int, max_total_ms: fl
 # hex digits of the sha256 of the kernel's source file when it was captured.
 # A source that has changed since makes the figure stale: it is reported as
 # null.  Captured with
-#   ncu --set full --clock-control none \
-#       -k regex:"indexer_kernel|topk_kernel|sparse_mla_kernel" -s 3 -c 3 \
+#   ncu --set full --clock-control none -k regex:<kernel>_kernel -s <n> -c <1..3> \
 #       -o <report> python bench.py --steps 5 --warmup 3 --no-per-config
+# (the exact command of each capture is kept with its ncu summary)
 NCU_TRAFFIC = {
     ("decode", "indexer"): ("indexer.cu", "5f358bf61f8aaa44", 273867264.0),
     ("decode", "topk"): ("topk.cu", "51834c3a49681375", 4273664.0),
-    ("decode", "sparse_mla"): ("sparse_mla.cu", "73585f896bfb16d3", 82764800.0),
+    ("decode", "sparse_mla"): ("sparse_mla.cu", "c4a76ec2f68182a4", 82548736.0),
 }
 
 
