@@ -486,12 +486,21 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
       // the maximum over all 64 keys (both threads of the row find the same),
       // the exponentials for this thread's 32
       // of the raw selected scores, scaled once: the scale is positive, so
-      // max(s) * scale = max(s * scale) under rounding as well
-      float mr = neg_inf();
+      // max(s) * scale = max(s * scale) under rounding as well.  The reference
+      // moves only when a selected score passes it by 2^8, which the maximum
+      // over all 64 keys bounds: the selection is consulted only when that
+      // passes (the first tiles of a row, or an unselected key far above it).
+      float ur = neg_inf();
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        mr = fmaxf(mr, ((c < 32 ? bits.x : bits.y) & (1u << (c & 31))) ? __uint_as_float(sv[c]) : neg_inf());
-      const float mt = mr * p.scale_log2;
+      for (int c = 0; c < 64; ++c) ur = fmaxf(ur, __uint_as_float(sv[c]));
+      float mt = ur * p.scale_log2;
+      if (mt > m_ref + 8.f) {
+        float mr = neg_inf();
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          mr = fmaxf(mr, ((c < 32 ? bits.x : bits.y) & (1u << (c & 31))) ? __uint_as_float(sv[c]) : neg_inf());
+        mt = mr * p.scale_log2;
+      }
       const uint32_t mine = hf ? bits.y : bits.x;
       // the reference moves when a score passes it by more than 2^8; O and l
       // follow it (TMEM loads and stores are warp-wide: a row that keeps its
