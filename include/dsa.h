@@ -201,6 +201,9 @@ dsa_status_t dsa_sparse_mla_fwd(const dsa_batch_t* batch, const dsa_mla_layer_t*
  *   outs   host array of n_layers device bf16 [total_q, n_heads, d_v] pointers.
  *   lses   host array of n_layers device fp32 [total_q, n_heads] pointers
  *          (entries may be NULL), or NULL.
+ *          Output and LSE buffers may also be pinned (page-locked) host
+ *          memory, which the device addresses directly: the results then land
+ *          in host memory with no copy back (each is written once).
  *   workspace  device, >= dsa_workspace_size(batch, topk) bytes.
  */
 dsa_status_t dsa_forward(const dsa_batch_t* batch, const dsa_indexer_t* indexer, int32_t topk,

@@ -57,3 +57,25 @@ def test_results_into_caller_buffers(lib, name, kw):
     assert torch.equal(idx, idx_ref)
     for a, b in zip(outs, outs_ref):
         assert torch.equal(a, b)
+
+
+def test_outputs_into_pinned_host_memory(lib):
+    # the sparse MLA writes outputs and LSE straight into pinned host memory
+    # (no copy back); they equal the device-memory results bit for bit
+    from long_context_lightning_gb300 import SparseAttention
+    spec = W.SPECS["ragged"].scaled(batch=7, ctx_range=(300, 6000))
+    wl = W.make_workload(spec, device="cuda")
+    ref = make_sa(wl)
+    idx_ref, outs_ref, lses_ref = ref.forward()
+    outs = [torch.full(o.shape, -1.0, dtype=o.dtype).pin_memory() for o in outs_ref]
+    lses = [torch.full(x.shape, -1.0, dtype=x.dtype).pin_memory() for x in lses_ref]
+    sa = SparseAttention(wl.cu_seqlens_q, wl.seq_lens, wl.q_idx, wl.w, wl.k_idx, wl.q, wl.kv, spec.d_v, spec.scale,
+                         spec.topk, page_table=wl.page_table, page_size=spec.page_size, outs=outs, lses=lses)
+    sa.forward()
+    torch.cuda.synchronize()
+    assert lib.check_device_error() == lib.DSA_OK
+    assert torch.equal(sa.idx, idx_ref)
+    for a, b in zip(outs, outs_ref):
+        assert torch.equal(a, b.cpu())
+    for a, b in zip(lses, lses_ref):
+        assert torch.equal(a, b.cpu())
