@@ -799,6 +799,7 @@ dsa_status_t dsa_mha_project(const void* latent, int64_t latent_stride, int64_t 
   a.k_out = k_out;
   a.v_out = v_out;
   a.err = dev.err;
+  a.num_sms = dev.num_sms;
   return launch_mha_project(a, stream) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -214,6 +214,7 @@ struct MhaProjectLaunch {
   void* k_out;        // bf16 [rows, H, 256]
   void* v_out;        // bf16 [rows, H, 256]
   int* err;
+  int num_sms;        // one persistent block per SM
 };
 struct MhaAttendLaunch {
   PlanView plan;      // groups of up to 128 queries

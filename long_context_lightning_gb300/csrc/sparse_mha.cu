@@ -51,9 +51,13 @@ struct ProjCfg {
   static constexpr int A_BYTES = 128 * 128;      // 128 rows x 64 dims
   static constexpr int B_BYTES = N * 128;        // N outputs x 64 dims
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int THREADS = 64 + 128;       // producer, MMA issuer, four epilogue warps
+  static constexpr int N_BARS = 2 * STAGES + 4 + 1;
   static constexpr int OFF_BAR = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * N_BARS;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(N % 16 == 0 && N <= 256, "tcgen05 M=128 needs N in [16, 256]");
+  static_assert(SMEM_BYTES <= 227 * 1024, "projection stages exceed shared memory");
 };
 
 struct ProjParams {
@@ -65,8 +69,14 @@ struct ProjParams {
   int* err;
 };
 
+// Persistent: one block per SM walks the (128-row tile, head) output tiles
+// t = blockIdx.x, + gridDim.x, ...  The producer streams the tiles' K blocks
+// (latent rows and the head's projection rows) through a ring of stages
+// across tile boundaries; the MMA issuer accumulates each tile into one of two
+// TMEM accumulators, so the epilogue of one tile (four warps, one row a
+// thread) overlaps the MMAs of the next.
 template <int N, bool KEYS>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(ProjCfg<N>::THREADS, 1)
     mha_project_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_w,
                        ProjParams p) {
   using C = ProjCfg<N>;
@@ -74,29 +84,34 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 8 * (2 * C::STAGES + 2));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   auto full = [&](int s) { return smem_u32(bars + s); };
   auto empty = [&](int s) { return smem_u32(bars + C::STAGES + s); };
-  const uint32_t done = smem_u32(bars + 2 * C::STAGES);
-  const uint32_t drain = smem_u32(bars + 2 * C::STAGES + 1);
+  auto acc_full = [&](int a) { return smem_u32(bars + 2 * C::STAGES + a); };
+  auto acc_empty = [&](int a) { return smem_u32(bars + 2 * C::STAGES + 2 + a); };
+  const uint32_t drain = smem_u32(bars + 2 * C::STAGES + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = blockIdx.x * 128, h = blockIdx.y;
+  const int n_rt = (int)((p.rows + 127) / 128);
+  const int n_tiles = n_rt * p.H;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 128);
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_c);
     prefetch_tmap(&tm_w);
   }
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 256);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 2 * N <= 256 ? 256 : 512);
     tmem_relinquish();
   }
   pdl_wait();  // the latent pool may come from the previous kernel on the stream
@@ -106,73 +121,94 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    int issued = 0;
-    for (int kb = 0; kb < C::KB; ++kb) {
-      const int s = kb % C::STAGES;
-      if (kb >= C::STAGES && !mbar_wait(empty(s), ((kb / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
-      const uint32_t dst = sbase + s * C::STAGE_BYTES;
-      mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
-      tma_load_2d(dst, &tm_c, full(s), kb * 64, r0);
-      tma_load_2d(dst + C::A_BYTES, &tm_w, full(s), kb * 64, h * N);
-      ++issued;
-    }
-    if (*abort_flag)  // the loads already issued land before the block leaves
-      for (int kb = std::max(0, issued - C::STAGES); kb < issued; ++kb)
-        mbar_wait_drain(full(kb % C::STAGES), (kb / C::STAGES) & 1);
-  } else if (warp == 1 && lane == 0) {
-    const uint32_t idesc = mma_idesc_bf16(128, N, false, false);
-    bool ok = true;
-    for (int kb = 0; kb < C::KB && ok; ++kb) {
-      const int s = kb % C::STAGES;
-      if (!(ok = mbar_wait(full(s), (kb / C::STAGES) & 1, abort_flag, p.err))) break;
-      tc_fence_after();
-      const uint32_t a0 = sbase + s * C::STAGE_BYTES, b0 = a0 + C::A_BYTES;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem, smem_desc_sw128(a0 + ks * 32, 16, 1024), smem_desc_sw128(b0 + ks * 32, 16, 1024), idesc,
-                 (kb | ks) != 0);
-      mma_commit(empty(s));
-    }
-    if (ok) mma_commit(done);
-    mma_commit(drain);  // every MMA of this thread done before TMEM is freed
-    mbar_wait_drain(drain, 0);
-  }
-  __syncwarp();
-
-  // epilogue: thread = one row of the tile (TMEM lane)
-  const bool ok = mbar_wait(done, 0, abort_flag, p.err);
-  tc_fence_after();
-  const int row = warp * 32 + lane;
-  const int64_t r = (int64_t)r0 + row;
-  if (ok) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < N; c0 += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + c0, v);
-      tmem_wait_ld();
-      if (r < p.rows) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + c0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]), __uint_as_float(v[8 * i + 1])),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int it = 0;  // K blocks issued, over all of this block's tiles
+      for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+        const int r0 = (t / p.H) * 128, h = t % p.H;
+        for (int kb = 0; kb < C::KB; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (it >= C::STAGES && !mbar_wait(empty(s), ((it / C::STAGES) - 1) & 1, abort_flag, p.err)) break;
+          const uint32_t dst = sbase + s * C::STAGE_BYTES;
+          mbar_arrive_expect_tx(full(s), C::STAGE_BYTES);
+          tma_load_2d(dst, &tm_c, full(s), kb * 64, r0);
+          tma_load_2d(dst + C::A_BYTES, &tm_w, full(s), kb * 64, h * N);
+        }
       }
+      if (*abort_flag)  // the loads already issued land before the block leaves
+        for (int j = std::max(0, it - C::STAGES); j < it; ++j)
+          mbar_wait_drain(full(j % C::STAGES), (j / C::STAGES) & 1);
     }
-    if (KEYS && r < p.rows) {  // the rope dims every head shares follow the head's no-rope dims
-      const uint4* src = reinterpret_cast<const uint4*>(p.c + r * p.c_stride + kLatent);
-      uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + N);
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = mma_idesc_bf16(128, N, false, false);
+      bool ok = true;
+      int it = 0, i = 0;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++i) {
+        const int a = i & 1;
+        // the epilogue has read this accumulator's previous tile
+        if (i >= 2 && !(ok = mbar_wait(acc_empty(a), ((i >> 1) - 1) & 1, abort_flag, p.err))) break;
+        tc_fence_after();
+        for (int kb = 0; kb < C::KB; ++kb, ++it) {
+          const int s = it % C::STAGES;
+          if (!(ok = mbar_wait(full(s), (it / C::STAGES) & 1, abort_flag, p.err))) break;
+          tc_fence_after();
+          const uint32_t a0 = sbase + s * C::STAGE_BYTES, b0 = a0 + C::A_BYTES;
 #pragma unroll
-      for (int i = 0; i < kRope / 8; ++i) dst[i] = __ldg(src + i);
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + a * N, smem_desc_sw128(a0 + ks * 32, 16, 1024), smem_desc_sw128(b0 + ks * 32, 16, 1024),
+                     idesc, (kb | ks) != 0);
+          mma_commit(empty(s));
+        }
+        if (ok) mma_commit(acc_full(a));
+      }
+      mma_commit(drain);  // every MMA of this thread done before TMEM is freed
+      mbar_wait_drain(drain, 0);
+    }
+  } else {
+    // ------------------------------------------- epilogue: one row a thread
+    const int quad = warp & 3;  // TMEM lanes 32 * quad .. + 31
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    int i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (!mbar_wait(acc_full(a), (i >> 1) & 1, abort_flag, p.err)) break;
+      tc_fence_after();
+      const int h = t % p.H;
+      const int64_t r = (int64_t)(t / p.H) * 128 + row;
+#pragma unroll 1
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(lane_base + a * N + c0, v);
+        tmem_wait_ld();
+        if (r < p.rows) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty(a));  // the accumulator may take the tile after next
+      if (KEYS && r < p.rows) {   // the rope dims every head shares follow the head's no-rope dims
+        const uint4* src = reinterpret_cast<const uint4*>(p.c + r * p.c_stride + kLatent);
+        uint4* dst = reinterpret_cast<uint4*>(p.out + (r * p.H + h) * kHead + N);
+#pragma unroll
+        for (int q = 0; q < kRope / 8; ++q) dst[q] = __ldg(src + q);
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 2 * N <= 256 ? 256 : 512);
   }
 }
 
@@ -631,8 +667,9 @@ cudaError_t launch_project_one(const MhaProjectLaunch& a, const void* w, __nv_bf
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   void* args[] = {&tm_c, &tm_w, &p};
-  const dim3 grid((unsigned)((a.rows + 127) / 128), (unsigned)a.H, 1);
-  return launch_with(reinterpret_cast<const void*>(kern), grid, 128, C::SMEM_BYTES, args, stream, true);
+  const int64_t n_tiles = (a.rows + 127) / 128 * a.H;
+  const dim3 grid((unsigned)std::min<int64_t>(n_tiles, a.num_sms), 1, 1);
+  return launch_with(reinterpret_cast<const void*>(kern), grid, C::THREADS, C::SMEM_BYTES, args, stream, true);
 }
 
 }  // namespace
