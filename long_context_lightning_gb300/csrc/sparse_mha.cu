@@ -307,8 +307,10 @@ __global__ void __launch_bounds__(AttCfg::THREADS, 1)
 
   pdl_wait();  // the plan and the masks are complete from here on
   pdl_trigger();
-  const int g = blockIdx.x, h = blockIdx.y;
-  if (g >= p.plan.header[0]) return;  // the grid is sized for the most groups a batch can have
+  // groups in reverse: a sequence's later groups see more keys (causal), so the
+  // longest blocks start first and the short ones fill the last wave
+  const int g = p.plan.header[0] - 1 - (int)blockIdx.x, h = blockIdx.y;
+  if (g < 0) return;  // the grid is sized for the most groups a batch can have
   const int4 gi = p.plan.g_info[g];   // {sequence, first query, queries, n of the last query}
   const int b = gi.x, q0 = gi.y, cnt = gi.z;
   const int n_kt = (gi.w + 63) / 64;
